@@ -1,0 +1,404 @@
+"""Throughput of the tiled dense matrix multiply on GB300.
+
+One step = the two products the headline metric is quoted on, each one call of
+the C entry point on inputs already resident in HBM:
+  * 8192 x 8192 x 8192, bf16 inputs, fp32 accumulate and output (tgemm_bf16);
+  * 4096 x 4096 x 4096, fp32 (tgemm_f32, FFMA).
+``value`` = their flops (2mnk each) / their summed device time, in TFLOP/s.
+Each launch is bracketed by CUDA events on the stream it runs on, and L2 is
+flushed (a 512 MiB write) before every launch, outside the events.
+
+The same JSON line carries, for information, the other measured shapes
+(4096^3 on the TF32 tensor-core path, 16 x 8192 x 8192 bf16, the
+4097 x 3001 x 1023 fp32 edge-tile case), a roofline object for the kernel
+taking most of the step's time, the end-to-end number through the C ABI from
+pinned host buffers, the CPU oracle timed on a bounded sample of the same
+workload, and the SM clocks sampled while timing.
+
+``--impl reference`` times the CPU oracle instead (a bounded sample of the
+same workload per step) and prints the same metric for it.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tgemm|reference]
+Under torchrun each rank runs its own copy of the step (weak scaling, no
+collective on the data path); rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOPS (2mnk/s) at 4096³ fp32 & 8192³ bf16; % of GB300 roofline"
+UNIT = "TFLOP/s"
+SM_COUNT = 152
+SM_MAX_MHZ = 2070.0
+FFMA_PEAK_TFLOPS = SM_COUNT * 128 * 2 * SM_MAX_MHZ * 1e6 / 1e12   # 80.54
+NOMINAL_BF16, NOMINAL_TF32 = 2250.0, 1100.0
+
+# name -> (workload, entry, dtype)
+PARTS = {
+    "bf16_8192": ("bf16_8192", "bf16", "bf16"),
+    "f32_4096": ("n4096", "f32", "f32"),
+}
+EXTRAS = {
+    "tf32_4096": ("n4096", "tf32", "f32"),
+    "skinny_bf16": ("skinny", "bf16", "bf16"),
+    "irregular_f32": ("irregular", "f32", "f32"),
+}
+KERNEL_NAMES = {"f32": "ffma_f32_kernel", "tf32": "umma_kernel<true>", "bf16": "umma_kernel<false>"}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def roofline_for(entry, case, seconds, peaks, peaks_src):
+    """Roofline object of one launch: skinny bf16 is HBM-bound, the rest compute-bound."""
+    flops = 2.0 * case.m * case.n * case.k
+    es = 2 if entry == "bf16" else 4
+    bytes_ = es * (case.m * case.k + case.k * case.n) + 4 * case.m * case.n
+    if case.m <= 64:
+        achieved = bytes_ / seconds / 1e9
+        peak = float(peaks["hbm_gbs"])
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_source": f"hbm_gbs of {peaks_src}", "algorithmic_bytes": int(bytes_)}
+    achieved = flops / seconds / 1e12
+    if entry == "f32":
+        peak, src = FFMA_PEAK_TFLOPS, "152 SMs x 128 FP32 lanes x 2 x 2070 MHz"
+        bound = "alu"
+    elif entry == "bf16":
+        peak, src = float(peaks["bf16_tflops"]), f"bf16_tflops (burst) of {peaks_src}"
+        bound = "tensor"
+    else:
+        peak = float(peaks["bf16_tflops"]) * NOMINAL_TF32 / NOMINAL_BF16
+        src = f"bf16_tflops (burst) of {peaks_src} x 1.1/2.25 (nominal tf32/bf16)"
+        bound = "tensor"
+    return {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4), "traffic": None, "peak_source": src,
+            "algorithmic_flops": int(flops)}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.device_index = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.device_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "tgemm" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value, world):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_sample(cases, target_s, max_rows=None):
+    """Times the oracle on the first r rows of each case, r doubled until the
+    run takes at least target_s / 4 seconds.  Returns (flops, seconds, rows, cores)."""
+    import oracle
+    cores = oracle.available_cores()
+    r = max(1, cores // 2)
+    while True:
+        t0 = time.perf_counter()
+        flops = 0
+        for c in cases:
+            rows = min(r, c.m)
+            oracle.gemm(c.A[:rows], c.B)
+            flops += 2 * rows * c.n * c.k
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 4 or (max_rows and r >= max_rows) or r >= min(c.m for c in cases):
+            return flops, dt, r, cores
+        r *= 2 if dt < target_s / 8 else 1
+        if dt >= target_s / 8:
+            r = max(r + 1, int(r * (target_s / 2) / max(dt, 1e-3)))
+
+
+def bench_reference(args, world, rank):
+    """The CPU oracle as it stands, on a bounded sample of the step's workload."""
+    from dense_tiled_matrix_gb300 import inputs
+    if rank != 0:
+        return
+    cases = [inputs.make(PARTS[p][0]) for p in PARTS]
+    flops, dt, rows, cores = cpu_sample(cases, target_s=8.0)
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        for c in cases:
+            import oracle
+            oracle.gemm(c.A[:rows], c.B)
+        if i >= args.warmup:
+            per_step.append(time.perf_counter() - t0)
+    total = sum(per_step)
+    value = flops * len(per_step) / total / 1e12
+    sample = f"first {rows} rows of each of 8192x8192x8192 bf16 and 4096x4096x4096 fp32 per step"
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total / len(per_step) * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64)",
+            "impl": "reference",
+            "config": {"workload": "gemm 8192^3 bf16->fp32 + 4096^3 fp32 (oracle sample)", "rows_per_part": rows,
+                       "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def bench_tgemm(args, world, rank, local):
+    import torch
+
+    from dense_tiled_matrix_gb300 import inputs, tgemm
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tgemm.load()
+    peaks, peaks_src = load_peaks()
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def to_dev(arr):
+        import numpy as np
+        if arr.dtype == np.uint16:
+            return torch.from_numpy(arr.view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(arr).to(dev)
+
+    case_cache = {}
+
+    def case_of(name):
+        if name not in case_cache:
+            case_cache[name] = inputs.make(name)
+        return case_cache[name]
+
+    def prepare(spec):
+        wl, entry, _ = spec
+        c = case_of(wl)
+        A = to_dev(inputs.convert(c, "bf16" if entry == "bf16" else "f32").A)
+        B = to_dev(inputs.convert(c, "bf16" if entry == "bf16" else "f32").B)
+        C = torch.empty((c.m, c.n), dtype=torch.float32, device=dev)
+        fn = {"f32": tgemm.tgemm_f32, "tf32": tgemm.tgemm_tf32, "bf16": tgemm.tgemm_bf16}[entry]
+        return c, A, B, C, fn
+
+    def timed(runs, iters):
+        """Per-launch device times (s) of `iters` rounds over `runs`, L2 flushed before each launch."""
+        times = {name: [] for name in runs}
+        for _ in range(iters):
+            for name, (c, A, B, C, fn) in runs.items():
+                flush.zero_()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn(A, B, C, stream)
+                e1.record(stream)
+                times[name].append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return {n: [a.elapsed_time(b) / 1e3 for a, b in v] for n, v in times.items()}
+
+    runs = {name: prepare(spec) for name, spec in PARTS.items()}
+    extras = {} if args.no_extras else {name: prepare(spec) for name, spec in EXTRAS.items()}
+
+    with ClockSampler(local) as clocks:
+        timed(runs, args.warmup)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        launches0 = tgemm.tgemm_kernel_launches()
+        t_wall0 = time.perf_counter()
+        per = timed(runs, args.steps)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+        launches = tgemm.tgemm_kernel_launches() - launches0
+        barrier(world)
+        extra_times = timed(extras, args.warmup + args.steps) if extras else {}
+    step_s = sum(sum(v) for v in per.values()) / args.steps
+    step_s = max_over_ranks(step_s, world)
+    flops_step = sum(2.0 * runs[n][0].m * runs[n][0].n * runs[n][0].k for n in runs)
+    value = world * flops_step / step_s / 1e12
+
+    parts = {}
+    for name, ts in list(per.items()) + [(n, v[args.warmup:]) for n, v in extra_times.items()]:
+        c = (runs.get(name) or extras.get(name))[0]
+        entry = (PARTS.get(name) or EXTRAS.get(name))[1]
+        avg = sum(ts) / len(ts)
+        parts[name] = {"m": c.m, "n": c.n, "k": c.k, "entry": f"tgemm_{entry}", "ms": round(avg * 1e3, 4),
+                       "tflops": round(2.0 * c.m * c.n * c.k / avg / 1e12, 2),
+                       "roofline": roofline_for(entry, c, avg, peaks, peaks_src)}
+    dominant = max(PARTS, key=lambda n: sum(per[n]))
+    roof = dict(parts[dominant]["roofline"])
+    roof["kernel"] = KERNEL_NAMES[PARTS[dominant][1]]
+    roof["workload"] = dominant
+
+    # End to end through the C ABI: pinned host inputs -> device, product, result -> host.
+    e2e = None
+    if not args.no_e2e:
+        host = {}
+        h2d = d2h = 0
+        for name, (c, A, B, C, fn) in runs.items():
+            hA = torch.empty(A.shape, dtype=A.dtype, pin_memory=True)
+            hB = torch.empty(B.shape, dtype=B.dtype, pin_memory=True)
+            hA.copy_(A)
+            hB.copy_(B)
+            hC = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
+            dA, dB, dC = torch.empty_like(A), torch.empty_like(B), torch.empty_like(C)
+            host[name] = (hA, hB, hC, dA, dB, dC, runs[name][4])
+            h2d += hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
+            d2h += hC.numel() * hC.element_size()
+
+        def e2e_step():
+            for hA, hB, hC, dA, dB, dC, fn in host.values():
+                dA.copy_(hA, non_blocking=True)
+                dB.copy_(hB, non_blocking=True)
+                fn(dA, dB, dC, stream)
+                hC.copy_(dC, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps, world)
+        e2e = {"value": round(world * flops_step / e2e_s / 1e12, 3), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e2e_s * 1e3, 3)}
+
+    status = tgemm.tgemm_get_device_status(stream)
+    if status != tgemm.TGEMM_OK:
+        raise RuntimeError(f"device status after the bench: {tgemm.tgemm_status_string(status)}")
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        flops, dt, rows, cores = cpu_sample([case_of(PARTS[p][0]) for p in PARTS], target_s=args.cpu_seconds)
+        cpu = {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"first {rows} rows of each of the step's two products (fp64 oracle), {dt:.1f} s"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32",
+                "data": "synthetic (seeded SplitMix64; bf16 N(0,1)/sqrt(k), fp32 N(0,1))",
+                "config": {"workload": "gemm 8192x8192x8192 bf16->fp32 (tcgen05) + 4096x4096x4096 fp32 (FFMA)",
+                           "l2": "flushed (512 MiB write) before every launch, outside the timed events",
+                           "parallelism": f"replicas x{world}"},
+                "roofline": roof, "parts": parts, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": int(launches), "clocks": clocks.summary(),
+                "wall_s_timed_region": round(t_wall, 3), "impl": "tgemm"}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["tgemm", "reference"], default="tgemm")
+    ap.add_argument("--no-extras", action="store_true", help="skip the informational extra shapes")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0, help="target length of the CPU-oracle sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        bench_reference(args, world, rank)
+    else:
+        bench_tgemm(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

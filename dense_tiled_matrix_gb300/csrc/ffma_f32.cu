@@ -1,0 +1,224 @@
+// ffma_f32.cu -- fp32 C = A * B on the FMA pipes (tgemm_f32).
+//
+// The tiled matrix multiply of hecess.blogspot.com "[Multi-Core & GPU
+// Programming] CUDA - Matrix Multiplication" (sections "[Shared Memory]" and
+// "Tiled Matrix Multiplication Kernel"), rebuilt for sm_103a:
+//
+//  * Output tiles.  Each CTA owns a 128 x 128 tile of C (the page's block owns
+//    a TILE_WIDTH x TILE_WIDTH tile); tiles are numbered in groups of 8 tile
+//    rows so that CTAs running together share A and B tiles in L2.
+//  * Phases.  K is walked in phases of BK = 16.  Instead of every thread
+//    copying one element and a __syncthreads, one thread issues two TMA bulk
+//    tensor copies per phase into a 4-stage ring of shared-memory tiles; an
+//    mbarrier per stage ("full") replaces the first __syncthreads (data has
+//    landed) and a second per stage ("empty", one arrival per warp) replaces
+//    the second one (nobody still reads the tile that the next copy
+//    overwrites).  Out-of-range rows and columns are zero-filled by TMA.
+//  * More outputs per thread (the page's remedy for unused shared memory, end
+//    of "Tile Size 결정"): 256 threads each keep an 8 x 8 block of C in
+//    registers (the page's Pvalue, 64 of them), so every shared-memory value
+//    read feeds 8 FMAs.
+//  * Bank conflicts (note.jhbae.stream "Lec 29 · GPU Architecture (2)": 32
+//    banks of 4 bytes, N-way conflicts replay, one word read by many threads is
+//    a broadcast).  A tiles (128 rows x 64 bytes) are stored with TMA's 64-byte
+//    swizzle; a warp's 128-bit reads of A touch 4 rows whose 16-byte chunks
+//    land in 4 distinct bank groups, and lanes reading the same row broadcast.
+//    B tiles (16 rows x 512 bytes) are stored plain; 8 consecutive lanes read
+//    128 consecutive bytes.  Both patterns take one shared-memory wavefront
+//    per instruction (checked by the host-side bank model in the tests).
+//  * Coalescing / corner turning (section "[Coalescing]"): TMA moves whole
+//    tile rows; the epilogue writes 4 rows x 128 contiguous bytes per warp
+//    instruction with 128-bit stores.
+//
+// Each C element is the sum over k, in ascending k, of fused multiply-adds
+// into one fp32 register that starts at 0, then stored once.
+#include <cstdio>
+
+#include "device.cuh"
+#include "host.h"
+
+namespace tgemm {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kBK = 16;
+constexpr int kStages = 4;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kGroupM = 8;
+constexpr uint32_t kStageA = kBM * kBK * 4;   // 8 KiB
+constexpr uint32_t kStageB = kBK * kBN * 4;   // 8 KiB
+constexpr size_t kSmemBytes = 1024 + kStages * (kStageA + kStageB) + 2 * kStages * sizeof(uint64_t);
+
+__device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& tm, int& tn) {
+    const int per_group = kGroupM * tiles_n;
+    const int group = tile / per_group;
+    const int first = group * kGroupM;
+    const int rows = min(tiles_m - first, kGroupM);
+    const int in_group = tile - group * per_group;
+    tm = first + in_group % rows;
+    tn = in_group / rows;
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                float* __restrict__ C, int64_t ldc, int M, int N, int K, int vec_store,
+                uint32_t* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    float* sA = reinterpret_cast<float*>(smem);
+    float* sB = reinterpret_cast<float*>(smem + kStages * kStageA);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * (kStageA + kStageB));
+    uint64_t* empty = full + kStages;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int tiles_m = (M + kBM - 1) / kBM;
+    const int tiles_n = (N + kBN - 1) / kBN;
+    int tile_m, tile_n;
+    tile_coords(blockIdx.x, tiles_m, tiles_n, tile_m, tile_n);
+    const int m0 = tile_m * kBM;
+    const int n0 = tile_n * kBN;
+    const int KT = (K + kBK - 1) / kBK;
+
+    if (tid == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (tid == 0) {
+        const int first = KT < kStages ? KT : kStages;
+        for (int s = 0; s < first; ++s) {
+            mbar_arrive_expect_tx(&full[s], kStageA + kStageB);
+            tma_load_2d(sA + s * (kBM * kBK), &tmA, &full[s], s * kBK, m0);
+            tma_load_2d(sB + s * (kBK * kBN), &tmB, &full[s], n0, s * kBK);
+        }
+    }
+
+    // Thread layout: warp (wm, wn) covers rows 32*wm .. +31 and columns
+    // 64*wn .. +63; lane (tm, tn) takes rows tm + 4i (i < 8) and columns
+    // 4*tn .. +3 and 32 + 4*tn .. +3 of that warp tile.
+    const int wm = warp >> 1, wn = warp & 1;
+    const int tm = lane >> 3, tn = lane & 7;
+    const int a_row0 = 32 * wm + tm;
+    const int b_col0 = 64 * wn + 4 * tn;
+    // 64-byte swizzle: 16-byte chunk c of tile row r sits at chunk c ^ ((r >> 1) & 3).
+    // For r = a_row0 + 4i this is (tm >> 1) ^ (2 * (i & 1)).
+    const int swz_even = tm >> 1;
+
+    float acc[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+
+    bool ok = true;
+    int s = 0;
+    uint32_t phase = 0;
+    for (int kt = 0; kt < KT; ++kt) {
+        // Refill the stage drained in the previous phase with phase kt-1+kStages.
+        if (tid == 0 && kt > 0) {
+            const int next = kt - 1 + kStages;
+            if (next < KT) {
+                const int ps = (kt - 1) % kStages;
+                const uint32_t pph = static_cast<uint32_t>((kt - 1) / kStages) & 1u;
+                if (!mbar_wait(&empty[ps], pph, status)) { ok = false; break; }
+                mbar_arrive_expect_tx(&full[ps], kStageA + kStageB);
+                tma_load_2d(sA + ps * (kBM * kBK), &tmA, &full[ps], next * kBK, m0);
+                tma_load_2d(sB + ps * (kBK * kBN), &tmB, &full[ps], n0, next * kBK);
+            }
+        }
+        if (!mbar_wait(&full[s], phase, status)) { ok = false; break; }
+
+        const float* As = sA + s * (kBM * kBK);
+        const float* Bs = sB + s * (kBK * kBN);
+#pragma unroll
+        for (int kc = 0; kc < kBK / 4; ++kc) {
+            float4 av[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = a_row0 + 4 * i;
+                const int chunk = kc ^ (swz_even ^ ((i & 1) << 1));
+                av[i] = *reinterpret_cast<const float4*>(As + r * kBK + chunk * 4);
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float* brow = Bs + (kc * 4 + kk) * kBN + b_col0;
+                const float4 b0 = *reinterpret_cast<const float4*>(brow);
+                const float4 b1 = *reinterpret_cast<const float4*>(brow + 32);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float a = kk == 0 ? av[i].x : kk == 1 ? av[i].y : kk == 2 ? av[i].z : av[i].w;
+                    acc[i][0] = fmaf(a, b0.x, acc[i][0]);
+                    acc[i][1] = fmaf(a, b0.y, acc[i][1]);
+                    acc[i][2] = fmaf(a, b0.z, acc[i][2]);
+                    acc[i][3] = fmaf(a, b0.w, acc[i][3]);
+                    acc[i][4] = fmaf(a, b1.x, acc[i][4]);
+                    acc[i][5] = fmaf(a, b1.y, acc[i][5]);
+                    acc[i][6] = fmaf(a, b1.z, acc[i][6]);
+                    acc[i][7] = fmaf(a, b1.w, acc[i][7]);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+        if (++s == kStages) { s = 0; phase ^= 1u; }
+    }
+    if (!ok) return;   // status already records the timeout; C is left unwritten
+
+    // Epilogue: every element written exactly once.
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int gm = m0 + a_row0 + 4 * i;
+        if (gm >= M) continue;
+        float* crow = C + static_cast<int64_t>(gm) * ldc;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int gn = n0 + b_col0 + 32 * h;
+            if (vec_store && gn + 3 < N) {
+                *reinterpret_cast<float4*>(crow + gn) =
+                    make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (gn + j < N) crow[gn + j] = acc[i][4 * h + j];
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_ffma_f32(const Problem& p, const Device& dev) {
+    CUtensorMap ta, tb;
+    if (!make_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.A, p.m, p.k, p.lda, kBM, kBK,
+                         CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.k, p.n, p.ldb, kBK, kBN,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(ffma_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(kSmemBytes));
+    if (err != cudaSuccess) {
+        set_error("cudaFuncSetAttribute(ffma_f32_kernel): %s", cudaGetErrorString(err));
+        return err;
+    }
+    const int64_t tiles = static_cast<int64_t>((p.m + kBM - 1) / kBM) * ((p.n + kBN - 1) / kBN);
+    const int vec_store = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
+    ffma_f32_kernel<<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, p.stream>>>(
+        ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status);
+    count_launch();
+    err = cudaGetLastError();
+    if (err != cudaSuccess) set_error("ffma_f32_kernel launch: %s", cudaGetErrorString(err));
+    return err;
+}
+
+}  // namespace tgemm

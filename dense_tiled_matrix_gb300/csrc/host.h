@@ -1,0 +1,68 @@
+// host.h -- declarations shared by the host parts of libtgemm: the per-device
+// context, the problem description handed to each kernel's launcher, and the
+// launchers themselves (one per kernel family, defined next to its kernel).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace tgemm {
+
+struct Device {
+    int ordinal = -1;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    int smem_optin = 0;           // max dynamic shared memory per block (bytes)
+    uint32_t* status = nullptr;   // device address of this device's status word
+};
+
+// One product C = A * B, row-major, as validated by the C entry points.
+// `A`/`B` point at fp32 or bf16 elements depending on the entry point.
+struct Problem {
+    int m = 0, n = 0, k = 0;
+    const void* A = nullptr;
+    int64_t lda = 0;
+    const void* B = nullptr;
+    int64_t ldb = 0;
+    float* C = nullptr;
+    int64_t ldc = 0;
+    cudaStream_t stream = nullptr;
+};
+
+// Counts a kernel launch made by the library.
+void count_launch();
+
+// Encodes a 2-D tiled TMA descriptor over a row-major matrix of `rows` x
+// `cols` elements (cols contiguous) with a row pitch of `ld` elements and a
+// box of `box_rows` x `box_cols`.  Returns false with a message on failure.
+bool make_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem_bytes,
+                     const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                     uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle);
+
+// Records a failure text for tgemm_last_error().
+void set_error(const char* fmt, ...);
+
+// ------------------------------------------------------------ launchers --
+// Each returns cudaSuccess or the launch error (with set_error called).
+
+// fp32 FFMA kernel; A and B must be 16-byte aligned with 16-byte row pitches.
+cudaError_t launch_ffma_f32(const Problem& p, const Device& dev);
+
+// tcgen05 kernels; same alignment rule.  `tf32` selects kind::tf32 on fp32
+// inputs, and then p.B must hold B TRANSPOSED (n x k, pitch p.ldb, k
+// contiguous); otherwise bf16 inputs under kind::f16 with B as k x n.
+cudaError_t launch_umma(const Problem& p, const Device& dev, bool tf32);
+
+// dst (cols x rows, pitch ld_dst) = transpose of src (rows x cols, pitch
+// ld_src), 4-byte elements.
+cudaError_t launch_transpose(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows,
+                             int64_t cols, cudaStream_t stream, const Device& dev);
+
+// Copies a rows x cols matrix of `elem_bytes`-byte elements with pitch `ld_src`
+// into `dst` with pitch `ld_dst` (elements), zero-filling columns
+// cols .. ld_dst-1.
+cudaError_t launch_pack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows,
+                        int64_t cols, int elem_bytes, cudaStream_t stream, const Device& dev);
+
+}  // namespace tgemm

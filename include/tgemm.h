@@ -1,0 +1,132 @@
+/*
+ * tgemm.h -- C ABI of libtgemm, the tiled dense matrix multiply for NVIDIA
+ * GB300 (sm_103a).
+ *
+ * The operation (hecess.blogspot.com "[Multi-Core & GPU Programming] CUDA -
+ * Matrix Multiplication", section "[Matrix Multiplication]", the loop that
+ * keeps the running sum in a register and writes P(i,j) once; generalised from
+ * the page's square Width x Width case to rectangular row-major matrices):
+ *
+ *     C[i*ldc + j] = sum_{kk=0}^{k-1} A[i*lda + kk] * B[kk*ldb + j]
+ *     for 0 <= i < m, 0 <= j < n.
+ *
+ * A is m x k, B is k x n and C is m x n, all row-major with leading dimensions
+ * (element strides between consecutive rows) lda, ldb and ldc -- the page's
+ * flattened indices M[row*width+k] and N[k*width+col] (section
+ * "[Coalescing]") with one "width" per matrix.  C is overwritten, never
+ * accumulated into.  k == 0 gives C = 0 (the empty sum).
+ *
+ * Memory and ownership.  A, B and C are DEVICE pointers (cudaMalloc'd or
+ * managed memory on the current device) owned by the caller; the library
+ * never frees them and keeps no reference after the call returns.  The
+ * library may take temporary stream-ordered workspace on `stream` (for
+ * operands whose base address or leading dimension is not a multiple of 16
+ * bytes) and returns it on the same stream.
+ *
+ * Execution.  Every call is asynchronous on `stream` (NULL is the legacy
+ * default stream) and returns once the work is queued.  Argument errors are
+ * found on the host before anything is queued.  A launch failure returns
+ * TGEMM_ERR_CUDA.  Faults during execution surface at the caller's next
+ * synchronisation; a kernel whose internal pipeline wait exceeds its time
+ * limit stops, records TGEMM_ERR_TIMEOUT in a per-device status word and
+ * exits, and tgemm_get_device_status() reports it.
+ *
+ * Results.  tgemm_f32 multiplies in fp32 with fused multiply-add (one
+ * rounding per term); tgemm_tf32 feeds fp32 inputs to the tensor cores as
+ * TF32 and accumulates in fp32; tgemm_bf16 takes bf16 inputs and accumulates
+ * and writes fp32.  Each element of C is written exactly once.  The order in
+ * which the k terms are added is fixed per shape, so repeated calls give
+ * bit-identical results.
+ *
+ * Thread safety.  All entry points may be called from several host threads
+ * at once.  Calls on different streams may overlap on the GPU; C of one call
+ * must not overlap A, B or C of a call that can run at the same time.
+ */
+#ifndef TGEMM_H
+#define TGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;   /* cudaStream_t is `struct CUstream_st *` */
+
+typedef enum tgemm_status {
+    TGEMM_OK = 0,
+    /* A size, leading dimension or pointer breaks the rules below, or C
+     * overlaps A or B. */
+    TGEMM_ERR_INVALID_VALUE = 1,
+    /* Reserved: misaligned operands are repacked, never rejected. */
+    TGEMM_ERR_MISALIGNED = 2,
+    /* The current device is not an sm_103 GPU (the kernels are built for
+     * sm_103a only; there is no fallback of any kind). */
+    TGEMM_ERR_UNSUPPORTED_DEVICE = 3,
+    /* A CUDA runtime or driver call failed; tgemm_last_error() has its text. */
+    TGEMM_ERR_CUDA = 4,
+    /* A kernel gave up on a pipeline wait after its time limit. */
+    TGEMM_ERR_TIMEOUT = 5,
+    /* Temporary workspace could not be allocated. */
+    TGEMM_ERR_WORKSPACE = 6
+} tgemm_status;
+
+/*
+ * Argument rules shared by the three products:
+ *   m, n, k >= 0 and each < 2^31;
+ *   lda >= max(1, k), ldb >= max(1, n), ldc >= max(1, n);
+ *   A may be NULL only when m == 0 or k == 0; B only when k == 0 or n == 0;
+ *   C only when m == 0 or n == 0;
+ *   non-NULL pointers are device or managed memory of the current device;
+ *   C[0 .. (m-1)*ldc + n) overlaps neither A's nor B's span.
+ * m == 0 or n == 0 is a no-op returning TGEMM_OK.
+ */
+
+/* fp32 x fp32 -> fp32 on the FMA pipes: register-blocked, TMA-staged tiles in
+ * bank-conflict-free shared memory fed through an mbarrier pipeline. */
+tgemm_status tgemm_f32(int64_t m, int64_t n, int64_t k,
+                       const float *A, int64_t lda,
+                       const float *B, int64_t ldb,
+                       float *C, int64_t ldc,
+                       struct CUstream_st *stream);
+
+/* fp32 inputs multiplied as TF32 on the tcgen05 tensor cores, fp32
+ * accumulation in tensor memory, fp32 output. */
+tgemm_status tgemm_tf32(int64_t m, int64_t n, int64_t k,
+                        const float *A, int64_t lda,
+                        const float *B, int64_t ldb,
+                        float *C, int64_t ldc,
+                        struct CUstream_st *stream);
+
+/* bf16 inputs (A and B point at IEEE bfloat16 values, 2 bytes each) on the
+ * tcgen05 tensor cores, fp32 accumulation, fp32 output.  For m <= 64 the
+ * product is formed as C^T = B^T A^T with the k range split across CTAs and
+ * the partial sums added in a fixed order. */
+tgemm_status tgemm_bf16(int64_t m, int64_t n, int64_t k,
+                        const void *A, int64_t lda,
+                        const void *B, int64_t ldb,
+                        float *C, int64_t ldc,
+                        struct CUstream_st *stream);
+
+/* Static English text of a status code (never NULL). */
+const char *tgemm_status_string(tgemm_status status);
+
+/* Text of the last failure seen by the calling host thread ("" if none). */
+const char *tgemm_last_error(void);
+
+/* Waits for `stream`, then reads and clears the current device's status word.
+ * Returns TGEMM_OK, TGEMM_ERR_TIMEOUT if a kernel gave up on a wait since the
+ * last read, or TGEMM_ERR_CUDA if the synchronisation itself failed. */
+tgemm_status tgemm_get_device_status(struct CUstream_st *stream);
+
+/* Kernels launched by this library in this process so far (all devices). */
+uint64_t tgemm_kernel_launches(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int tgemm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TGEMM_H */

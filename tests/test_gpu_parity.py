@@ -1,0 +1,135 @@
+"""GPU parity: every entry point against the CPU oracle, through the C ABI.
+
+Small and medium cases are compared element by element over the whole
+output; the full-size workloads (4096^3 fp32, 8192^3 bf16) on sampled rows and
+entries that the oracle evaluates one by one.  Integer-valued inputs must match
+exactly; other inputs within the bounds stated in ``parity.py``.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dense_tiled_matrix_gb300 import inputs, tgemm
+import parity
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["f32", "tf32", "bf16"]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    tgemm.load()
+    yield
+    assert tgemm.tgemm_get_device_status() == tgemm.TGEMM_OK
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("name", ["worked_4x4", "int64", "u128", "int1024"])
+def test_named_small_cases(mode, name):
+    parity.full_check(mode, inputs.make(name))
+
+
+EDGE_SHAPES = [
+    (1, 1, 1), (1, 7, 3), (5, 1, 9), (2, 3, 300), (127, 129, 33), (128, 128, 16), (128, 256, 64),
+    (129, 257, 17), (255, 300, 31), (300, 200, 1), (513, 300, 100), (64, 1000, 129),
+    (1000, 64, 65), (257, 511, 257), (130, 260, 520),
+]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", EDGE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_edge_tiles(mode, shape):
+    m, n, k = shape
+    parity.full_check(mode, inputs.random_case(2000 + m + 7 * n + 13 * k, m, n, k, kind="int"),
+                      f"{mode} int {shape}")
+    parity.full_check(mode, inputs.random_case(3000 + m + 7 * n + 13 * k, m, n, k, kind="uniform"),
+                      f"{mode} uniform {shape}")
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_irregular_4097x3001x1023(mode):
+    # lda = 1023 and ldb = ldc = 3001: no row pitch is a multiple of 16 bytes.
+    parity.full_check(mode, inputs.make("irregular"))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_leading_dimensions_and_untouched_padding(mode):
+    m, n, k = 200, 150, 90
+    case = inputs.random_case(4242, m, n, k, kind="int")
+    A_np, B_np = parity.inputs_for(mode, case)
+    dtype = torch.bfloat16 if mode == "bf16" else torch.float32
+    A_big = torch.zeros((m, k + 13), dtype=dtype, device="cuda")
+    B_big = torch.zeros((k, n + 6), dtype=dtype, device="cuda")
+    A_big[:, 5:5 + k] = parity.to_device(A_np)
+    B_big[:, :n] = parity.to_device(B_np)
+    C_big = torch.full((m, n + 10), float("nan"), device="cuda")
+    A, B, C = A_big[:, 5:5 + k], B_big[:, :n], C_big[:, 3:3 + n]
+    parity.ENTRY[mode](A, B, C)
+    torch.cuda.synchronize()
+    P, D = oracle.gemm(A_np, B_np)
+    parity.check(mode, C.cpu().numpy(), P, D, True, f"{mode} strided")
+    host = C_big.cpu().numpy()
+    assert np.all(np.isnan(host[:, :3])) and np.all(np.isnan(host[:, 3 + n:])), "wrote outside C"
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_k_zero_gives_zeros(mode):
+    dtype = torch.bfloat16 if mode == "bf16" else torch.float32
+    A = torch.empty((7, 0), dtype=dtype, device="cuda")
+    B = torch.empty((0, 5), dtype=dtype, device="cuda")
+    C = torch.full((7, 5), 3.0, device="cuda")
+    parity.ENTRY[mode](A, B, C)
+    torch.cuda.synchronize()
+    assert torch.all(C == 0)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_repeat_runs_are_bit_identical(mode):
+    case = inputs.random_case(555, 1000, 700, 900, kind="normal")
+    A_np, B_np = parity.inputs_for(mode, case)
+    A, B = parity.to_device(A_np), parity.to_device(B_np)
+    c1 = parity.ENTRY[mode](A, B)
+    c2 = parity.ENTRY[mode](A, B)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
+
+
+def _sampled_check(mode, case, n_rows, n_entries, seed):
+    A_np, B_np = parity.inputs_for(mode, case)
+    C = parity.run(mode, A_np, B_np)
+    m, n = C.shape
+    rng = np.random.default_rng(seed)
+    rows = sorted(set([0, 1, 127, 128, 129, m // 2, m - 1] + rng.integers(0, m, n_rows).tolist()))
+    Csub = C[torch.tensor(rows, device=C.device)].cpu().numpy()
+    P, D = oracle.gemm(A_np[rows], B_np)
+    err_rows = parity.check(mode, Csub, P, D, case.exact, f"{mode} {case} rows")
+    ri = rng.integers(0, m, n_entries)
+    ci = rng.integers(0, n, n_entries)
+    Pe, De = oracle.gemm_entries(A_np, B_np, ri, ci)
+    got = C[torch.from_numpy(ri).to(C.device), torch.from_numpy(ci).to(C.device)].cpu().numpy()
+    err_ent = parity.check(mode, got.reshape(-1, 1), Pe.reshape(-1, 1), De.reshape(-1, 1), case.exact,
+                           f"{mode} {case} entries")
+    return max(err_rows, err_ent)
+
+
+@pytest.fixture(scope="module")
+def case_n4096():
+    return inputs.make("n4096")
+
+
+@pytest.mark.parametrize("mode", ["f32", "tf32"])
+def test_full_size_4096_fp32(mode, case_n4096):
+    _sampled_check(mode, case_n4096, 24, 2000, 11)
+
+
+def test_full_size_8192_bf16():
+    _sampled_check("bf16", inputs.make("bf16_8192"), 8, 1000, 12)
+
+
+def test_skinny_16x8192x8192_bf16():
+    parity.full_check("bf16", inputs.make("skinny"))
