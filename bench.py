@@ -113,6 +113,10 @@ class ClockSampler:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.device_index}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            # wait (up to 5 s) for the first sample so the timed region is covered
+            t0 = time.time()
+            while time.time() - t0 < 5.0 and os.path.getsize(self.path) == 0:
+                time.sleep(0.05)
         except OSError:
             self.proc = None
         return self
@@ -148,6 +152,7 @@ class ClockSampler:
         power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "reasons": sorted(reasons), "samples": len(rows),
+                "window": "warm-up, timed steps and extra shapes (nvidia-smi every 100 ms)",
                 "power_w_max": max(power) if power else None}
 
 
@@ -380,7 +385,7 @@ def bench_tgemm(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tgemm", "reference"], default="tgemm")
     ap.add_argument("--no-extras", action="store_true", help="skip the informational extra shapes")

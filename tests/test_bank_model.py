@@ -1,0 +1,133 @@
+"""Shared-memory bank model and the kernels' access patterns, on the CPU.
+
+The model is the one the pages give (note.jhbae.stream "Lec 29 · GPU
+Architecture (2)", shared-memory banks; coffeejoa.com "CUDA.3 Writing CUDA
+SIMT Kernels", "Shared Memory Bank Conflict"): 32 banks of 4 bytes,
+consecutive words in consecutive banks, one word per bank per cycle; threads
+that read the same word share it (broadcast); threads that read different
+words of one bank are served one after another (an N-way conflict costs N
+passes).  A 16-byte access covers four consecutive banks.  The number of
+passes ("wavefronts") of a warp-wide access is the largest number of
+distinct words any bank must deliver.
+
+The FFMA kernel's addressing is restated here from its source and checked to
+need one pass per instruction; the TMA 64-byte swizzle it relies on is
+checked against the kernel's own chunk formula.
+"""
+import pytest
+
+BANKS = 32
+
+
+def wavefronts(addresses, width=4):
+    """Passes needed for one warp access: ``addresses`` are byte addresses, one per thread."""
+    words_per_bank = {}
+    for a in addresses:
+        for w in range(a // 4, (a + width) // 4):
+            words_per_bank.setdefault(w % BANKS, set()).add(w)
+    return max(len(v) for v in words_per_bank.values())
+
+
+def test_quiz_word_1_and_word_33_conflict():
+    # Thread 0 reads word 1, thread 1 reads word 33: both in bank 1 -> 2-way conflict.
+    assert wavefronts([1 * 4, 33 * 4]) == 2
+
+
+def test_stride_one_and_broadcast_are_conflict_free():
+    assert wavefronts([4 * t for t in range(32)]) == 1
+    assert wavefronts([4 * 7] * 32) == 1
+    # bytes of the same word do not conflict either
+    assert wavefronts([4 * 3 + (t % 4) for t in range(32)]) == 1
+
+
+def test_transpose_tile_column_read_without_and_with_padding():
+    # tile[32][32]: a warp reading one column hits one bank 32 times (31 replays).
+    col = 5
+    assert wavefronts([(r * 32 + col) * 4 for r in range(32)]) == 32
+    # tile[32][33]: the extra word shifts each row by one bank -> conflict-free.
+    assert wavefronts([(r * 33 + col) * 4 for r in range(32)]) == 1
+    # the row read stays conflict-free with the padding
+    assert wavefronts([(7 * 33 + c) * 4 for c in range(32)]) == 1
+
+
+def swizzle64(offset):
+    """TMA 64-byte swizzle: bits [4,5] of the byte offset XOR bits [7,8]."""
+    return offset ^ (((offset >> 7) & 3) << 4)
+
+
+# ---- FFMA kernel (csrc/ffma_f32.cu): 128x16 fp32 A tile, 16x128 fp32 B tile ----
+BK, BN = 16, 128
+
+
+def ffma_lane(warp, lane):
+    wm, wn = warp >> 1, warp & 1
+    tm, tn = lane >> 3, lane & 7
+    return wm, wn, tm, tn
+
+
+def ffma_a_offset(warp, lane, i, kc):
+    """Byte offset in the A stage read by (warp, lane) for its row i and 16-byte chunk kc."""
+    wm, wn, tm, tn = ffma_lane(warp, lane)
+    r = 32 * wm + tm + 4 * i
+    chunk = kc ^ ((tm >> 1) ^ ((i & 1) << 1))
+    return (r * BK + chunk * 4) * 4
+
+
+def ffma_b_offset(warp, lane, k, half):
+    wm, wn, tm, tn = ffma_lane(warp, lane)
+    return (k * BN + 64 * wn + 4 * tn + 32 * half) * 4
+
+
+def test_ffma_a_chunk_formula_is_the_tma_swizzle():
+    for warp in range(8):
+        for lane in range(32):
+            wm, wn, tm, tn = ffma_lane(warp, lane)
+            for i in range(8):
+                r = 32 * wm + tm + 4 * i
+                for kc in range(4):
+                    logical = r * 64 + kc * 16
+                    assert ffma_a_offset(warp, lane, i, kc) == swizzle64(logical)
+
+
+@pytest.mark.parametrize("warp", range(8))
+def test_ffma_a_reads_take_one_pass(warp):
+    for i in range(8):
+        for kc in range(4):
+            addrs = [ffma_a_offset(warp, lane, i, kc) for lane in range(32)]
+            assert wavefronts(addrs, width=16) == 1, (warp, i, kc)
+
+
+def test_ffma_a_reads_would_conflict_without_the_swizzle():
+    # Same rows, unswizzled layout: rows 4 apart share bank groups.
+    worst = 0
+    for i in range(8):
+        for kc in range(4):
+            addrs = []
+            for lane in range(32):
+                wm, wn, tm, tn = ffma_lane(0, lane)
+                r = 32 * wm + tm + 4 * i
+                addrs.append(r * 64 + kc * 16)
+            worst = max(worst, wavefronts(addrs, width=16))
+    assert worst > 1
+
+
+@pytest.mark.parametrize("warp", range(8))
+def test_ffma_b_reads_take_one_pass(warp):
+    for k in range(BK):
+        for half in range(2):
+            addrs = [ffma_b_offset(warp, lane, k, half) for lane in range(32)]
+            assert wavefronts(addrs, width=16) == 1, (warp, k, half)
+
+
+def test_ffma_thread_tiles_cover_the_cta_tile_once():
+    seen = set()
+    for warp in range(8):
+        for lane in range(32):
+            wm, wn, tm, tn = ffma_lane(warp, lane)
+            for i in range(8):
+                for h in range(2):
+                    for j in range(4):
+                        cell = (32 * wm + tm + 4 * i, 64 * wn + 4 * tn + 32 * h + j)
+                        assert cell not in seen
+                        seen.add(cell)
+    assert seen == {(r, c) for r in range(128) for c in range(128)}
