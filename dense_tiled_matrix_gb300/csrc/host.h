@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "tgemm.h"
+
 namespace tgemm {
 
 struct Device {
@@ -40,8 +42,23 @@ bool make_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem_
                      const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
                      uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swizzle);
 
-// Records a failure text for tgemm_last_error().
+// Records a failure text for tgemm_last_error(); clear_error() empties it.
 void set_error(const char* fmt, ...);
+void clear_error();
+
+// Host-side checks shared by the entry points (tgemm_api.cu).
+// The current device, set up on first use (sm_103 check, SM count, status word).
+tgemm_status current_device(Device** out);
+// `p` is device or managed memory of device `ord` and [p, p + bytes) lies in one allocation.
+tgemm_status check_span(const char* name, const void* p, uint64_t bytes, int ord);
+// Records "what: <CUDA error text>" and returns TGEMM_ERR_CUDA.
+tgemm_status cuda_fail(const char* what, cudaError_t err);
+// TMA can describe the matrix: 16-byte aligned base and 16-byte row pitch.
+bool tma_ok(const void* p, int64_t ld, int es);
+// Bytes spanned by a rows x cols row-major matrix with pitch ld.
+uint64_t span_bytes(int64_t rows, int64_t cols, int64_t ld, int es);
+// The byte ranges [a, a+na) and [b, b+nb) intersect.
+bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb);
 
 // ------------------------------------------------------------ launchers --
 // Each returns cudaSuccess or the launch error (with set_error called).

@@ -60,6 +60,8 @@ Device g_devices[kMaxDevices];
 tgemm_status g_dev_state[kMaxDevices];   // TGEMM_OK once set up; error otherwise
 bool g_dev_ready[kMaxDevices];
 
+}  // namespace
+
 tgemm_status cuda_fail(const char* what, cudaError_t err) {
     set_error("%s: %s", what, cudaGetErrorString(err));
     return TGEMM_ERR_CUDA;
@@ -166,6 +168,8 @@ bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + nb && y < x + na;
 }
+
+namespace {
 
 tgemm_status run(Kind kind, int64_t m, int64_t n, int64_t k, const void* A, int64_t lda, const void* B,
                  int64_t ldb, float* C, int64_t ldc, cudaStream_t stream) {
@@ -302,6 +306,8 @@ void set_error(const char* fmt, ...) {
 }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+void clear_error() { t_last_error[0] = '\0'; }
 
 bool make_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint32_t elem_bytes, const void* base,
                      uint64_t rows, uint64_t cols, uint64_t ld, uint32_t box_rows, uint32_t box_cols,

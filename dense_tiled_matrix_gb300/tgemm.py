@@ -31,6 +31,7 @@ SIGNATURES = {
     "tgemm_f32": (ctypes.c_int, _GEMM_ARGS),
     "tgemm_tf32": (ctypes.c_int, _GEMM_ARGS),
     "tgemm_bf16": (ctypes.c_int, _GEMM_ARGS),
+    "tgemm_tf32_noalloc": (ctypes.c_int, _GEMM_ARGS),
     "tgemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tgemm_last_error": (ctypes.c_char_p, []),
     "tgemm_get_device_status": (ctypes.c_int, [_VP]),
@@ -124,6 +125,16 @@ def tgemm_bf16(A, B, C=None, stream=None):
     """C (float32) = A @ B for bfloat16 tensors on the tensor cores, fp32 accumulation."""
     import torch
     return _call("tgemm_bf16", A, B, C, stream, torch.bfloat16)
+
+
+def tgemm_tf32_noalloc(A, B, C=None, stream=None):
+    """Like ``tgemm_tf32`` but with its scratch in the library's static device
+    array (no allocation by the library); the shape must fit TGEMM_NOALLOC_SCRATCH_BYTES."""
+    import torch
+    return _call("tgemm_tf32_noalloc", A, B, C, stream, torch.float32)
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 def tgemm_status_string(status: int) -> str:

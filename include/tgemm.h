@@ -108,6 +108,43 @@ tgemm_status tgemm_bf16(int64_t m, int64_t n, int64_t k,
                         float *C, int64_t ldc,
                         struct CUstream_st *stream);
 
+/* Size of the static device array used by tgemm_tf32_noalloc (32 MiB). */
+#define TGEMM_NOALLOC_SCRATCH_BYTES (32ull << 20)
+
+/*
+ * tgemm_tf32 without allocating.  Same operation, argument rules, results and
+ * status codes as tgemm_tf32 (the pages have no counterpart: this concerns only
+ * where the library keeps its temporary data).
+ *
+ * Who needs it: callers that cannot let a library allocate device memory --
+ * programs whose device memory is wholly managed by their own allocator or a
+ * fixed arena, and hot paths that must not pay for, or synchronise on, an
+ * allocation.  tgemm_tf32 takes a transposed copy of B (and, for a misaligned
+ * A, a re-pitched copy of A) from the stream-ordered allocator on each call;
+ * this entry point keeps them in a static device array of
+ * TGEMM_NOALLOC_SCRATCH_BYTES instead, and calls no allocation routine.
+ *
+ * Limit: the shape must need at most TGEMM_NOALLOC_SCRATCH_BYTES of scratch,
+ * namely 4 * n * k4 bytes plus 4 * m * k4 more when A's base address or lda*4
+ * is not a multiple of 16 (k4 = k rounded up to a multiple of 4, each part
+ * rounded up to 256 bytes); a larger shape returns TGEMM_ERR_INVALID_VALUE
+ * before any work is queued, with the sizes in tgemm_last_error().
+ *
+ * The array: one copy per GPU that loads the library, held until the process
+ * exits.  The first call on a device looks up its device address (with that
+ * device current), which also makes CUDA load it; make that first call before
+ * any stream capture.  All calls on a device share the one array and it keeps
+ * whatever the last call left in it (nothing in it needs to start at zero), so
+ * two calls whose GPU work can overlap -- on different streams, or on one
+ * stream from different threads without ordering -- race on it.  Serialise
+ * them, for example by issuing them on one stream.
+ */
+tgemm_status tgemm_tf32_noalloc(int64_t m, int64_t n, int64_t k,
+                                const float *A, int64_t lda,
+                                const float *B, int64_t ldb,
+                                float *C, int64_t ldc,
+                                struct CUstream_st *stream);
+
 /* Static English text of a status code (never NULL). */
 const char *tgemm_status_string(tgemm_status status);
 
