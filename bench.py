@@ -5,8 +5,12 @@ the C entry point on inputs already resident in HBM:
   * 8192 x 8192 x 8192, bf16 inputs, fp32 accumulate and output (tgemm_bf16);
   * 4096 x 4096 x 4096, fp32 (tgemm_f32, FFMA).
 ``value`` = their flops (2mnk each) / their summed device time, in TFLOP/s.
-Each launch is bracketed by CUDA events on the stream it runs on, and L2 is
-flushed (a 512 MiB write) before every launch, outside the events.
+Each launch is bracketed by CUDA events on the stream it runs on.  L2 hygiene:
+inputs larger than L2 -- every shape keeps R copies of its inputs (R copies
+>= 384 MiB, about 3x the 129 MB L2) and each launch reads the next copy, so no
+launch finds its operands in L2.  (A write-flush between launches was not used:
+it leaves ~129 MB of dirty lines that are written back during the next kernel,
+which penalises memory-bound kernels for work they did not do.)
 
 The same JSON line carries, for information, the other measured shapes
 (4096^3 on the TF32 tensor-core path, 16 x 8192 x 8192 bf16, the
@@ -53,7 +57,12 @@ EXTRAS = {
     "tf32_4096": ("n4096", "tf32", "f32"),
     "skinny_bf16": ("skinny", "bf16", "bf16"),
     "irregular_f32": ("irregular", "f32", "f32"),
+    # the pages' own kernels (libtgemm_pages), for the naive -> tiled comparison
+    "pages_naive_4096": ("n4096", "pages_naive", "f32"),
+    "pages_tiled16_4096": ("n4096", "pages_tiled16", "f32"),
+    "pages_tiled32_4096": ("n4096", "pages_tiled32", "f32"),
 }
+SLOW_EXTRA_ITERS = 4   # timed launches of the pages' kernels (tens of ms each)
 KERNEL_NAMES = {"f32": "ffma_f32_kernel", "tf32": "umma_kernel<true>", "bf16": "umma_kernel<false>"}
 
 
@@ -79,7 +88,7 @@ def roofline_for(entry, case, seconds, peaks, peaks_src):
                 "frac": round(achieved / peak, 4), "traffic": None,
                 "peak_source": f"hbm_gbs of {peaks_src}", "algorithmic_bytes": int(bytes_)}
     achieved = flops / seconds / 1e12
-    if entry == "f32":
+    if entry == "f32" or entry.startswith("pages"):
         peak, src = FFMA_PEAK_TFLOPS, "152 SMs x 128 FP32 lanes x 2 x 2070 MHz"
         bound = "alu"
     elif entry == "bf16":
@@ -240,14 +249,14 @@ def bench_reference(args, world, rank):
 def bench_tgemm(args, world, rank, local):
     import torch
 
-    from dense_tiled_matrix_gb300 import inputs, tgemm
+    from dense_tiled_matrix_gb300 import inputs, pages, tgemm
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     tgemm.load()
     peaks, peaks_src = load_peaks()
     stream = torch.cuda.current_stream(dev)
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    rotate_bytes = 384 * 2 ** 20
 
     def to_dev(arr):
         import numpy as np
@@ -265,18 +274,27 @@ def bench_tgemm(args, world, rank, local):
     def prepare(spec):
         wl, entry, _ = spec
         c = case_of(wl)
-        A = to_dev(inputs.convert(c, "bf16" if entry == "bf16" else "f32").A)
-        B = to_dev(inputs.convert(c, "bf16" if entry == "bf16" else "f32").B)
+        cc = inputs.convert(c, "bf16" if entry == "bf16" else "f32")
+        A0, B0 = to_dev(cc.A), to_dev(cc.B)
+        per_copy = A0.numel() * A0.element_size() + B0.numel() * B0.element_size()
+        R = max(1, -(-rotate_bytes // per_copy))
+        copies = [(A0, B0)] + [(A0.clone(), B0.clone()) for _ in range(R - 1)]
         C = torch.empty((c.m, c.n), dtype=torch.float32, device=dev)
-        fn = {"f32": tgemm.tgemm_f32, "tf32": tgemm.tgemm_tf32, "bf16": tgemm.tgemm_bf16}[entry]
-        return c, A, B, C, fn
+        fn = {"f32": tgemm.tgemm_f32, "tf32": tgemm.tgemm_tf32, "bf16": tgemm.tgemm_bf16,
+              "pages_naive": lambda A, B, C, st: pages.tgemm_pages_naive_f32(A, B, C, st),
+              "pages_tiled16": lambda A, B, C, st: pages.tgemm_pages_tiled_f32(A, B, C, 16, st),
+              "pages_tiled32": lambda A, B, C, st: pages.tgemm_pages_tiled_f32(A, B, C, 32, st)}[entry]
+        return c, copies, C, fn
 
-    def timed(runs, iters):
-        """Per-launch device times (s) of `iters` rounds over `runs`, L2 flushed before each launch."""
+    def timed(runs, iters, start=0, iters_of=None):
+        """Per-launch device times (s) of `iters` launches of each of `runs`; launch i reads copy i mod R."""
         times = {name: [] for name in runs}
-        for _ in range(iters):
-            for name, (c, A, B, C, fn) in runs.items():
-                flush.zero_()
+        # each shape in its own back-to-back run, so no launch inherits another
+        # shape's dirty output lines in L2
+        for name, (c, copies, C, fn) in runs.items():
+            n_it = (iters_of or {}).get(name, iters)
+            for it in range(start, start + n_it):
+                A, B = copies[it % len(copies)]
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -295,12 +313,13 @@ def bench_tgemm(args, world, rank, local):
         torch.cuda.synchronize(dev)
         launches0 = tgemm.tgemm_kernel_launches()
         t_wall0 = time.perf_counter()
-        per = timed(runs, args.steps)
+        per = timed(runs, args.steps, start=args.warmup)
         torch.cuda.synchronize(dev)
         t_wall = time.perf_counter() - t_wall0
         launches = tgemm.tgemm_kernel_launches() - launches0
         barrier(world)
-        extra_times = timed(extras, args.warmup + args.steps) if extras else {}
+        slow = {n: args.warmup + SLOW_EXTRA_ITERS for n in extras if n.startswith("pages")}
+        extra_times = timed(extras, args.warmup + args.steps, iters_of=slow) if extras else {}
     step_s = sum(sum(v) for v in per.values()) / args.steps
     step_s = max_over_ranks(step_s, world)
     flops_step = sum(2.0 * runs[n][0].m * runs[n][0].n * runs[n][0].k for n in runs)
@@ -311,7 +330,8 @@ def bench_tgemm(args, world, rank, local):
         c = (runs.get(name) or extras.get(name))[0]
         entry = (PARTS.get(name) or EXTRAS.get(name))[1]
         avg = sum(ts) / len(ts)
-        parts[name] = {"m": c.m, "n": c.n, "k": c.k, "entry": f"tgemm_{entry}", "ms": round(avg * 1e3, 4),
+        parts[name] = {"m": c.m, "n": c.n, "k": c.k, "entry": f"tgemm_{entry}", "launches_timed": len(ts),
+                       "ms": round(avg * 1e3, 4),
                        "tflops": round(2.0 * c.m * c.n * c.k / avg / 1e12, 2),
                        "roofline": roofline_for(entry, c, avg, peaks, peaks_src)}
     dominant = max(PARTS, key=lambda n: sum(per[n]))
@@ -324,14 +344,15 @@ def bench_tgemm(args, world, rank, local):
     if not args.no_e2e:
         host = {}
         h2d = d2h = 0
-        for name, (c, A, B, C, fn) in runs.items():
+        for name, (c, copies, C, fn) in runs.items():
+            A, B = copies[0]
             hA = torch.empty(A.shape, dtype=A.dtype, pin_memory=True)
             hB = torch.empty(B.shape, dtype=B.dtype, pin_memory=True)
             hA.copy_(A)
             hB.copy_(B)
             hC = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
             dA, dB, dC = torch.empty_like(A), torch.empty_like(B), torch.empty_like(C)
-            host[name] = (hA, hB, hC, dA, dB, dC, runs[name][4])
+            host[name] = (hA, hB, hC, dA, dB, dC, runs[name][3])
             h2d += hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
             d2h += hC.numel() * hC.element_size()
 
@@ -374,7 +395,7 @@ def bench_tgemm(args, world, rank, local):
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32",
                 "data": "synthetic (seeded SplitMix64; bf16 N(0,1)/sqrt(k), fp32 N(0,1))",
                 "config": {"workload": "gemm 8192x8192x8192 bf16->fp32 (tcgen05) + 4096x4096x4096 fp32 (FFMA)",
-                           "l2": "flushed (512 MiB write) before every launch, outside the timed events",
+                           "l2": "inputs larger than L2: each launch reads the next of R input copies (>= 384 MiB per shape)",
                            "parallelism": f"replicas x{world}"},
                 "roofline": roof, "parts": parts, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": int(launches), "clocks": clocks.summary(),

@@ -19,6 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libtgemm.so")
+PAGES_DIR = os.path.join(PKG, "csrc_pages")
+PAGES_LIB_PATH = os.path.join(PKG, "libtgemm_pages.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -35,13 +37,13 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found (set CUDA_HOME or put nvcc on PATH)")
 
 
-def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+def sources(directory=CSRC):
+    return sorted(os.path.join(directory, f) for f in os.listdir(directory) if f.endswith(".cu"))
 
 
 def _headers():
     hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
-    hs.append(os.path.join(INCLUDE, "tgemm.h"))
+    hs += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     return hs
 
 
@@ -52,16 +54,14 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile and link ``libtgemm.so``; returns its path."""
+def _build_lib(srcs, lib_path, tag, verbose, force, ptxas_verbose):
     os.makedirs(BUILD_DIR, exist_ok=True)
     cc = nvcc()
     headers = _headers()
-    srcs = sources()
     objs = []
     jobs = []
     for src in srcs:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD_DIR, tag + "_" + os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src, *headers, __file__]):
             cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
@@ -80,16 +80,26 @@ def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = Fals
                     sys.stderr.write(" ".join(cmd) + "\n" + res.stdout + res.stderr)
                 if res.returncode != 0:
                     raise RuntimeError(f"nvcc failed on {cmd[-3]}")
-    if force or jobs or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + ".tmp"
+    if force or jobs or _stale(lib_path, objs):
+        tmp = lib_path + ".tmp"
         cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-ldl", "-lpthread", "-lrt"]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if verbose or res.returncode != 0:
             sys.stderr.write(" ".join(cmd) + "\n" + res.stdout + res.stderr)
         if res.returncode != 0:
-            raise RuntimeError("linking libtgemm.so failed")
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+            raise RuntimeError(f"linking {os.path.basename(lib_path)} failed")
+        os.replace(tmp, lib_path)
+    return lib_path
+
+
+def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False) -> str:
+    """Compile and link ``libtgemm.so`` (and the pages' comparator library); returns libtgemm's path."""
+    with ThreadPoolExecutor(max_workers=2) as pool:
+        main = pool.submit(_build_lib, sources(), LIB_PATH, "tgemm", verbose, force, ptxas_verbose)
+        pages = pool.submit(_build_lib, sources(PAGES_DIR), PAGES_LIB_PATH, "pages", verbose, force,
+                            ptxas_verbose)
+        pages.result()
+        return main.result()
 
 
 if __name__ == "__main__":

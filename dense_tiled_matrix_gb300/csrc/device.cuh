@@ -62,8 +62,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits until the phase with the given parity of `bar` has completed.
 // Returns false (after recording kStatusTimeout) if that takes longer than
-// kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+// `limit_ns` (kWaitLimitNs unless given).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_addr(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t start = global_timer_ns();
@@ -71,7 +72,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(a, parity)) return true;
-        if (global_timer_ns() - start > kWaitLimitNs) {
+        if (global_timer_ns() - start > limit_ns) {
             atomicCAS(status, 0u, kStatusTimeout);
             return false;
         }
@@ -191,5 +192,48 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t ab_format, uint32_t a
 constexpr uint32_t kFormatBF16 = 1u;   // under kind::f16
 constexpr uint32_t kFormatTF32 = 2u;   // under kind::tf32
 constexpr uint32_t kSwizzle128B = 2u;
+
+}  // namespace tgemm
+
+namespace tgemm {
+
+// ---------------------------------------------------- thread-block clusters --
+
+__device__ __forceinline__ uint32_t cluster_cta_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Shared-memory address of the same variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t local_saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_saddr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_saddr) : "memory");
+    return v;
+}
+
+// Every thread of every CTA of the cluster must call this (it is the
+// cluster-wide counterpart of __syncthreads, with release/acquire ordering of
+// shared-memory writes).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's tensor-memory lane.
+__device__ __forceinline__ void tmem_load_16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
 
 }  // namespace tgemm

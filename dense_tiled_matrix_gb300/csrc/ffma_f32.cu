@@ -17,7 +17,8 @@
 //  * More outputs per thread (the page's remedy for unused shared memory, end
 //    of "Tile Size 결정"): 256 threads each keep an 8 x 8 block of C in
 //    registers (the page's Pvalue, 64 of them), so every shared-memory value
-//    read feeds 8 FMAs.
+//    read feeds 8 FMAs.  Pairs of neighbouring columns are updated with
+//    Blackwell's paired FMA (fma.rn.f32x2), halving the FMA instruction count.
 //  * Bank conflicts (note.jhbae.stream "Lec 29 · GPU Architecture (2)": 32
 //    banks of 4 bytes, N-way conflicts replay, one word read by many threads is
 //    a broadcast).  A tiles (128 rows x 64 bytes) are stored with TMA's 64-byte
@@ -61,7 +62,7 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
     tn = in_group / rows;
 }
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
 ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 float* __restrict__ C, int64_t ldc, int M, int N, int K, int vec_store,
                 uint32_t* status) {
@@ -115,11 +116,15 @@ ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     // For r = a_row0 + 4i this is (tm >> 1) ^ (2 * (i & 1)).
     const int swz_even = tm >> 1;
 
-    float acc[8][8];
+    // acc[i][p]: row a_row0 + 4i, columns b_col0 + 2p, +1 (p < 2) and
+    // b_col0 + 32 + 2(p-2), +1 (p >= 2).  Pairs of columns are updated by one
+    // paired FMA (fma.rn.f32x2): each lane is an ordinary fused multiply-add
+    // with one rounding, exactly as fmaf.
+    float2 acc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+        for (int p = 0; p < 4; ++p) acc[i][p] = make_float2(0.0f, 0.0f);
 
     bool ok = true;
     int s = 0;
@@ -141,31 +146,35 @@ ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
         const float* As = sA + s * (kBM * kBK);
         const float* Bs = sB + s * (kBK * kBN);
+        // Per 4 k-values: the thread's rows in two halves of 4 (i = 4h .. 4h+3),
+        // one 128-bit A read per row (4 consecutive k), two 128-bit B reads per k.
 #pragma unroll
         for (int kc = 0; kc < kBK / 4; ++kc) {
-            float4 av[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int r = a_row0 + 4 * i;
-                const int chunk = kc ^ (swz_even ^ ((i & 1) << 1));
-                av[i] = *reinterpret_cast<const float4*>(As + r * kBK + chunk * 4);
-            }
+            for (int half = 0; half < 2; ++half) {
+                float4 av[4];
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const float* brow = Bs + (kc * 4 + kk) * kBN + b_col0;
-                const float4 b0 = *reinterpret_cast<const float4*>(brow);
-                const float4 b1 = *reinterpret_cast<const float4*>(brow + 32);
+                for (int ii = 0; ii < 4; ++ii) {
+                    const int i = 4 * half + ii;
+                    const int r = a_row0 + 4 * i;
+                    const int chunk = kc ^ (swz_even ^ ((i & 1) << 1));
+                    av[ii] = *reinterpret_cast<const float4*>(As + r * kBK + chunk * 4);
+                }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float a = kk == 0 ? av[i].x : kk == 1 ? av[i].y : kk == 2 ? av[i].z : av[i].w;
-                    acc[i][0] = fmaf(a, b0.x, acc[i][0]);
-                    acc[i][1] = fmaf(a, b0.y, acc[i][1]);
-                    acc[i][2] = fmaf(a, b0.z, acc[i][2]);
-                    acc[i][3] = fmaf(a, b0.w, acc[i][3]);
-                    acc[i][4] = fmaf(a, b1.x, acc[i][4]);
-                    acc[i][5] = fmaf(a, b1.y, acc[i][5]);
-                    acc[i][6] = fmaf(a, b1.z, acc[i][6]);
-                    acc[i][7] = fmaf(a, b1.w, acc[i][7]);
+                for (int kk = 0; kk < 4; ++kk) {
+                    const float* brow = Bs + (kc * 4 + kk) * kBN + b_col0;
+                    const float4 b0 = *reinterpret_cast<const float4*>(brow);
+                    const float4 b1 = *reinterpret_cast<const float4*>(brow + 32);
+                    const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                                          make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
+#pragma unroll
+                    for (int ii = 0; ii < 4; ++ii) {
+                        const float a = kk == 0 ? av[ii].x : kk == 1 ? av[ii].y : kk == 2 ? av[ii].z : av[ii].w;
+                        const float2 aa = make_float2(a, a);
+#pragma unroll
+                        for (int p = 0; p < 4; ++p)
+                            acc[4 * half + ii][p] = __ffma2_rn(aa, bp[p], acc[4 * half + ii][p]);
+                    }
                 }
             }
         }
@@ -184,13 +193,13 @@ ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int gn = n0 + b_col0 + 32 * h;
+            const float v[4] = {acc[i][2 * h].x, acc[i][2 * h].y, acc[i][2 * h + 1].x, acc[i][2 * h + 1].y};
             if (vec_store && gn + 3 < N) {
-                *reinterpret_cast<float4*>(crow + gn) =
-                    make_float4(acc[i][4 * h], acc[i][4 * h + 1], acc[i][4 * h + 2], acc[i][4 * h + 3]);
+                *reinterpret_cast<float4*>(crow + gn) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    if (gn + j < N) crow[gn + j] = acc[i][4 * h + j];
+                    if (gn + j < N) crow[gn + j] = v[j];
             }
         }
     }

@@ -71,6 +71,10 @@ cudaError_t launch_ffma_f32(const Problem& p, const Device& dev);
 // contiguous); otherwise bf16 inputs under kind::f16 with B as k x n.
 cudaError_t launch_umma(const Problem& p, const Device& dev, bool tf32);
 
+// bf16 tcgen05 kernel for m <= 64: C^T = B^T A^T with k split across the CTAs
+// of a cluster and the partials added through distributed shared memory.
+cudaError_t launch_umma_skinny(const Problem& p, const Device& dev);
+
 // dst (cols x rows, pitch ld_dst) = transpose of src (rows x cols, pitch
 // ld_src), 4-byte elements.
 cudaError_t launch_transpose(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows,

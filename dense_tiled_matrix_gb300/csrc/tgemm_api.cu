@@ -280,6 +280,8 @@ tgemm_status run(Kind kind, int64_t m, int64_t n, int64_t k, const void* A, int6
             st = TGEMM_ERR_INVALID_VALUE;
         } else if (kind == Kind::F32) {
             err = launch_ffma_f32(p, *dev);
+        } else if (kind == Kind::BF16 && m <= 64) {
+            err = launch_umma_skinny(p, *dev);
         } else {
             err = launch_umma(p, *dev, kind == Kind::TF32);
         }

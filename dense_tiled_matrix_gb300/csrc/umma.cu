@@ -187,6 +187,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             const uint32_t acc_ph = (it >> 1) & 1;
             if (!mbar_wait(&acc_full[acc], acc_ph, status)) break;
             tc_fence_after_sync();
+            __syncwarp();   // tcgen05.ld below is warp-collective
             int tm, tn;
             tile_coords(tile, tiles_m, tiles_n, G::GROUP_M, tm, tn);
             const int row = tm * G::BM + quarter * 32 + lane;

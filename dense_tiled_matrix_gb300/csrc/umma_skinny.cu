@@ -1,0 +1,238 @@
+// umma_skinny.cu -- bf16 C = A * B for m <= 64 (tgemm_bf16 on short, wide A).
+//
+// With only m <= 64 rows of C there are too few 128 x 256 output tiles to
+// occupy the GPU, and the product is bound by streaming B (k x n) from HBM
+// once.  This kernel therefore
+//
+//  * forms the transposed product C^T = B^T A^T, so that n (large) is the
+//    tensor core's M dimension (128 columns of C per CTA) and m is its N
+//    dimension (16, 32 or 64).  B^T is read as stored: n contiguous, i.e. an
+//    MN-major operand; A is read as stored: k contiguous, K-major;
+//  * splits k across the S CTAs of a thread-block cluster (grid n/128 x S,
+//    cluster 1 x S), each streaming its k-slice of B through a 4-stage TMA
+//    ring (two 64 x 64 boxes of B and one NM x 64 box of A per stage) into
+//    tcgen05.mma, with the partial 128 x NM sums in tensor memory.  S is
+//    chosen so that about 5/3 CTAs per SM stream B;
+//  * adds the S partial sums through distributed shared memory (coffeejoa.com
+//    "CUDA.3 Writing CUDA SIMT Kernels", "Distributed Shared Memory": the
+//    cluster's shared memories form one address space, cluster.sync aligns the
+//    CTAs): every CTA parks its partial in its own shared memory, the cluster
+//    synchronises, and CTA r adds row m of all S partials, in rank order
+//    0..S-1, for the rows m = r, r+S, ... and writes them to C with coalesced
+//    stores.  No workspace, no atomics: the result is deterministic.
+//
+// All mbarrier waits are bounded (a timeout records TGEMM_ERR_TIMEOUT and
+// skips the remaining work), and every CTA always reaches both cluster
+// barriers, so no CTA can be left waiting for another.
+#include "device.cuh"
+#include "host.h"
+
+namespace tgemm {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kBK = 64;                     // k per stage (128 bytes of bf16)
+constexpr int kUK = 16;                     // k per MMA
+constexpr int kTileN = 128;                 // columns of C per CTA (tensor-core M)
+constexpr uint32_t kChunkBytes = kBK * 128; // one 64-column box of B: 64 k-rows x 128 bytes
+constexpr uint32_t kStageB = 2 * kChunkBytes;
+constexpr int kMaxSplit = 8;
+// k is split until about 5/3 CTAs per SM stream B (measured best on GB300
+// for 32..128 column tiles: 8 splits of 32 tiles, 4 of 64, 2 of 128).
+constexpr int kTargetCtasPer3Sms = 5;
+
+template <int NM>
+struct SkinnyCfg {
+    static constexpr uint32_t STAGE_A = NM * 128;                       // NM rows x 64 bf16
+    // 4 stages keep the CTA at ~75 KiB of shared memory; measured on GB300,
+    // deeper rings (8-12 stages, one CTA per SM) stream B more slowly overall.
+    static constexpr int STAGES = 4;
+    static constexpr uint32_t TMEM_COLS = NM < 32 ? 32 : NM;
+    static constexpr uint32_t IDESC = instr_desc(kFormatBF16, 1, 0, kTileN, NM);
+    static constexpr size_t SMEM = 1024 + STAGES * (kStageB + STAGE_A) + (2 * STAGES + 1) * 8 + 16;
+    static_assert(NM * kTileN * 4 <= STAGES * kStageB, "partial sums must fit in the B stages");
+};
+
+template <int NM>
+__global__ void __launch_bounds__(kThreads, 1)
+umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   float* __restrict__ C, int64_t ldc, int M, int N, int K, int kb_per_split,
+                   uint32_t* status) {
+    using G = SkinnyCfg<NM>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint8_t* sB = smem;                                   // STAGES x 16 KiB
+    uint8_t* sA = smem + G::STAGES * kStageB;               // STAGES x NM*128 B
+    uint64_t* full = reinterpret_cast<uint64_t*>(sA + G::STAGES * G::STAGE_A);
+    uint64_t* empty = full + G::STAGES;
+    uint64_t* done = empty + G::STAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+    // After the k loop the B stages hold this CTA's partial sums: red[m][j], j < 128.
+    float* red = reinterpret_cast<float*>(sB);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_cta_rank();
+    const uint32_t splits = gridDim.y;
+    const int n0 = blockIdx.x * kTileN;
+    const int KT = (K + kBK - 1) / kBK;
+    const int kb0 = static_cast<int>(rank) * kb_per_split;
+    const int kb1 = min(KT, kb0 + kb_per_split);
+    const int nkb = kb1 > kb0 ? kb1 - kb0 : 0;
+
+    if (threadIdx.x == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+        for (int s = 0; s < G::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(done, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, G::TMEM_COLS);
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    bool ok = true;
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------- TMA producer --
+        int s = 0;
+        uint32_t ph = 0;
+        for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&empty[s], ph ^ 1u, status)) { ok = false; break; }
+            mbar_arrive_expect_tx(&full[s], kStageB + G::STAGE_A);
+            uint8_t* b_dst = sB + s * kStageB;
+            tma_load_2d(b_dst, &tmB, &full[s], n0, kb * kBK);
+            tma_load_2d(b_dst + kChunkBytes, &tmB, &full[s], n0 + 64, kb * kBK);
+            tma_load_2d(sA + s * G::STAGE_A, &tmA, &full[s], kb * kBK, 0);
+            if (++s == G::STAGES) { s = 0; ph ^= 1u; }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ----------------------------------------------------- MMA issuer --
+        int s = 0;
+        uint32_t ph = 0;
+        for (int i = 0; i < nkb; ++i) {
+            if (!mbar_wait(&full[s], ph, status)) { ok = false; break; }
+            tc_fence_after_sync();
+            const uint32_t b0 = smem_addr(sB + s * kStageB);
+            const uint32_t a0 = smem_addr(sA + s * G::STAGE_A);
+#pragma unroll
+            for (int kk = 0; kk < kBK / kUK; ++kk) {
+                // tensor-core A = B^T: MN-major, 64-column chunks kChunkBytes apart,
+                // 8-row k groups 1 KiB apart; slice kk starts kUK rows down.
+                const uint64_t ad = smem_desc(b0 + kk * kUK * 128, kChunkBytes, 1024, kSwizzle128B);
+                // tensor-core B = A^T: K-major rows of 128 bytes, 8-row groups 1 KiB apart.
+                const uint64_t bd = smem_desc(a0 + kk * 32, 16, 1024, kSwizzle128B);
+                umma_f16(tmem, ad, bd, G::IDESC, (i | kk) != 0);
+            }
+            umma_commit(&empty[s]);
+            if (++s == G::STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (ok) umma_commit(done);
+    }
+
+    // ------------------------------------- partial sums -> shared memory --
+    __syncwarp();
+    bool have = nkb > 0;
+    if (have && !mbar_wait(done, 0, status)) have = false;
+    tc_fence_after_sync();
+    __syncwarp();   // tcgen05.ld is warp-collective
+    const int jrow = warp * 32 + lane;   // tensor-memory lane = column n0 + jrow of C
+    if (NM == 16) {
+        uint32_t r[16];
+        tmem_load_16(tmem + (static_cast<uint32_t>(warp * 32) << 16), r);
+        tmem_load_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) red[j * kTileN + jrow] = have ? __uint_as_float(r[j]) : 0.0f;
+    } else {
+#pragma unroll
+        for (int c = 0; c < NM / 32; ++c) {
+            uint32_t r[32];
+            tmem_load_32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c * 32, r);
+            tmem_load_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) red[(c * 32 + j) * kTileN + jrow] = have ? __uint_as_float(r[j]) : 0.0f;
+        }
+    }
+    tc_fence_before_sync();
+    __syncwarp();
+    cluster_sync_all();
+
+    // --------------------------- add the S partials in rank order, store --
+    const int rows = M < NM ? M : NM;
+    const int n = n0 + static_cast<int>(threadIdx.x);
+    const uint32_t my_red = smem_addr(red);
+    for (int mr = static_cast<int>(rank); mr < rows; mr += static_cast<int>(splits)) {
+        const uint32_t off = static_cast<uint32_t>((mr * kTileN + static_cast<int>(threadIdx.x)) * 4);
+        float sum = 0.0f;
+        for (uint32_t q = 0; q < splits; ++q) sum += ld_cluster_f32(cluster_map(my_red + off, q));
+        if (n < N) C[static_cast<int64_t>(mr) * ldc + n] = sum;
+    }
+    __syncwarp();
+    cluster_sync_all();   // partials stay readable until every CTA is done with them
+
+    if (warp == 0) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, G::TMEM_COLS);
+    }
+    (void)ok;
+}
+
+template <int NM>
+cudaError_t launch_nm(const Problem& p, const Device& dev) {
+    using G = SkinnyCfg<NM>;
+    CUtensorMap ta, tb;
+    if (!make_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.A, p.m, p.k, p.lda, NM, kBK,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.k, p.n, p.ldb, kBK, 64,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    auto kernel = umma_skinny_kernel<NM>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(G::SMEM));
+    if (err != cudaSuccess) {
+        set_error("cudaFuncSetAttribute(umma_skinny_kernel): %s", cudaGetErrorString(err));
+        return err;
+    }
+    const int tiles = (p.n + kTileN - 1) / kTileN;
+    const int KT = (p.k + kBK - 1) / kBK;
+    const int target = kTargetCtasPer3Sms * dev.sm_count / 3;
+    int splits = (target + tiles / 2) / tiles;
+    splits = splits < 1 ? 1 : splits;
+    splits = splits > kMaxSplit ? kMaxSplit : splits;
+    splits = splits > KT ? KT : splits;
+    const int kb_per_split = (KT + splits - 1) / splits;
+    splits = (KT + kb_per_split - 1) / kb_per_split;   // no empty slices
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(splits), 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = G::SMEM;
+    cfg.stream = p.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = static_cast<unsigned>(splits);
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kernel, ta, tb, p.C, p.ldc, p.m, p.n, p.k, kb_per_split, dev.status);
+    count_launch();
+    if (err != cudaSuccess) set_error("umma_skinny_kernel launch: %s", cudaGetErrorString(err));
+    return err;
+}
+
+}  // namespace
+
+cudaError_t launch_umma_skinny(const Problem& p, const Device& dev) {
+    if (p.m <= 16) return launch_nm<16>(p, dev);
+    if (p.m <= 32) return launch_nm<32>(p, dev);
+    return launch_nm<64>(p, dev);
+}
+
+}  // namespace tgemm

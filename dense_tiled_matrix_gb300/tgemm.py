@@ -35,6 +35,7 @@ SIGNATURES = {
     "tgemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tgemm_last_error": (ctypes.c_char_p, []),
     "tgemm_get_device_status": (ctypes.c_int, [_VP]),
+    "tgemm_selftest_wait_timeout": (ctypes.c_int, [_I64, _VP]),
     "tgemm_kernel_launches": (ctypes.c_uint64, []),
     "tgemm_version": (ctypes.c_int, []),
 }
@@ -148,6 +149,11 @@ def tgemm_last_error() -> str:
 def tgemm_get_device_status(stream=None) -> int:
     """Waits for ``stream`` and returns (and clears) the device status word."""
     return int(load().tgemm_get_device_status(_stream_handle(stream)))
+
+
+def tgemm_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    """Queues a kernel whose bounded wait must time out after ``limit_ns``; returns the call status."""
+    return int(load().tgemm_selftest_wait_timeout(int(limit_ns), _stream_handle(stream)))
 
 
 def tgemm_kernel_launches() -> int:

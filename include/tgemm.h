@@ -156,6 +156,16 @@ const char *tgemm_last_error(void);
  * last read, or TGEMM_ERR_CUDA if the synchronisation itself failed. */
 tgemm_status tgemm_get_device_status(struct CUstream_st *stream);
 
+/* Test of the failure path (the pages have no counterpart).  Queues on
+ * `stream` a one-thread kernel that waits, with the same bounded wait the
+ * product kernels use but a limit of `limit_ns` nanoseconds (1e3 .. 1e9), on a
+ * barrier that nothing ever arrives at.  The kernel gives up after the limit,
+ * records TGEMM_ERR_TIMEOUT in the device status word and returns, so a
+ * following tgemm_get_device_status() must report TGEMM_ERR_TIMEOUT and the
+ * CUDA context stays usable.  Returns TGEMM_OK once the kernel is queued,
+ * TGEMM_ERR_INVALID_VALUE for a limit outside the range. */
+tgemm_status tgemm_selftest_wait_timeout(int64_t limit_ns, struct CUstream_st *stream);
+
 /* Kernels launched by this library in this process so far (all devices). */
 uint64_t tgemm_kernel_launches(void);
 

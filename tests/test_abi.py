@@ -7,10 +7,11 @@ import re
 import pytest
 
 from dense_tiled_matrix_gb300 import build as tbuild
-from dense_tiled_matrix_gb300 import tgemm
+from dense_tiled_matrix_gb300 import pages, tgemm
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "tgemm.h")
+PAGES_HEADER = os.path.join(ROOT, "include", "tgemm_pages.h")
 
 
 @pytest.fixture(scope="module")
@@ -19,10 +20,34 @@ def lib():
     return tgemm.load()
 
 
-def declared_functions():
-    text = open(HEADER).read()
+def declared_functions(header=HEADER):
+    text = open(header).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(tgemm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_header_under_include_is_checked():
+    headers = sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
+    assert headers == ["tgemm.h", "tgemm_pages.h"]
+
+
+def test_pages_library_exports_its_header():
+    tbuild.build()
+    lib = pages.load()
+    names = declared_functions(PAGES_HEADER)
+    assert names == sorted(pages.SIGNATURES)
+    for name in names:
+        assert hasattr(lib, name)
+
+
+def test_pages_argument_rules_on_host():
+    tbuild.build()
+    lib = pages.load()
+    bad = tgemm.TGEMM_ERR_INVALID_VALUE
+    assert lib.tgemm_pages_tiled_f32(4, 4, 4, 16, 4, 32, 4, 64, 4, 8, None) == bad     # tile 8
+    assert lib.tgemm_pages_naive_f32(-1, 4, 4, 16, 4, 32, 4, 64, 4, None) == bad
+    assert lib.tgemm_pages_naive_f32(4, 4, 8, 16, 7, 32, 4, 64, 4, None) == bad      # lda < k
+    assert lib.tgemm_pages_naive_f32(0, 4, 4, None, 4, None, 4, None, 4, None) == tgemm.TGEMM_OK
 
 
 def test_header_declares_the_entry_points():
