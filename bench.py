@@ -197,50 +197,53 @@ def max_over_ranks(value, world):
 
 
 def cpu_sample(cases, target_s, max_rows=None):
-    """Times the oracle on the first r rows of each case, r doubled until the
-    run takes at least target_s / 4 seconds.  Returns (flops, seconds, rows, cores)."""
+    """Times the oracle on the first r rows of each case, growing r until one
+    pass takes about target_s seconds.  Returns (flops, seconds, rows, cores)."""
     import oracle
     cores = oracle.available_cores()
-    r = max(1, cores // 2)
+    limit = min(c.m for c in cases) if max_rows is None else min(max_rows, min(c.m for c in cases))
+    r = min(max(1, cores // 2), limit)
     while True:
         t0 = time.perf_counter()
         flops = 0
         for c in cases:
-            rows = min(r, c.m)
-            oracle.gemm(c.A[:rows], c.B)
-            flops += 2 * rows * c.n * c.k
+            oracle.gemm(c.A[:r], c.B)
+            flops += 2 * r * c.n * c.k
         dt = time.perf_counter() - t0
-        if dt >= target_s / 4 or (max_rows and r >= max_rows) or r >= min(c.m for c in cases):
+        if dt >= 0.5 * target_s or r >= limit:
             return flops, dt, r, cores
-        r *= 2 if dt < target_s / 8 else 1
-        if dt >= target_s / 8:
-            r = max(r + 1, int(r * (target_s / 2) / max(dt, 1e-3)))
+        grow = int(r * min(8.0, 0.8 * target_s / max(dt, 1e-3)))
+        r = min(limit, max(r + 1, grow))
 
 
 def bench_reference(args, world, rank):
-    """The CPU oracle as it stands, on a bounded sample of the step's workload."""
+    """The CPU oracle as it stands, on a bounded sample of the step's workload:
+    each step runs it on the first r rows of both products, r sized so the
+    whole run (warm-up + timed steps) takes about --ref-seconds."""
+    import oracle
     from dense_tiled_matrix_gb300 import inputs
     if rank != 0:
         return
     cases = [inputs.make(PARTS[p][0]) for p in PARTS]
-    flops, dt, rows, cores = cpu_sample(cases, target_s=8.0)
+    per_step_target = max(0.05, args.ref_seconds / (args.warmup + args.steps))
+    flops, dt, rows, cores = cpu_sample(cases, target_s=per_step_target)
     per_step = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
         for c in cases:
-            import oracle
             oracle.gemm(c.A[:rows], c.B)
         if i >= args.warmup:
             per_step.append(time.perf_counter() - t0)
     total = sum(per_step)
     value = flops * len(per_step) / total / 1e12
-    sample = f"first {rows} rows of each of 8192x8192x8192 bf16 and 4096x4096x4096 fp32 per step"
+    sample = (f"first {rows} rows of each of 8192x8192x8192 bf16 and 4096x4096x4096 fp32 per step "
+              f"(fp64 oracle, {cores} threads)")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total / len(per_step) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64)",
             "impl": "reference",
-            "config": {"workload": "gemm 8192^3 bf16->fp32 + 4096^3 fp32 (oracle sample)", "rows_per_part": rows,
-                       "l2": "n/a (CPU)"},
+            "config": {"workload": "gemm 8192x8192x8192 bf16->fp32 + 4096x4096x4096 fp32 (oracle row sample)",
+                       "rows_per_part": rows, "l2": "n/a (CPU)"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -413,6 +416,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     ap.add_argument("--cpu-seconds", type=float, default=20.0, help="target length of the CPU-oracle sample")
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="--impl reference: target length of the whole oracle run (warm-up + steps)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
