@@ -41,14 +41,17 @@
 namespace tgemm {
 namespace {
 
-constexpr int kBM = 128;
+constexpr int kWarpRows = 4;             // warps stacked along M, each 32 rows x 64 columns
+constexpr int kBM = 32 * kWarpRows;
 constexpr int kBN = 128;
 constexpr int kBK = 16;
 constexpr int kStages = 4;
-constexpr int kThreads = 256;
+constexpr int kThreads = 64 * kWarpRows;
 constexpr int kWarps = kThreads / 32;
+constexpr int kRowGroup = 4;             // rows of a thread processed together (4 or 8)
+constexpr int kChunkUnroll = 4;          // unrolling of the 4-wide k chunks of a stage (1..4)
 constexpr int kGroupM = 8;
-constexpr uint32_t kStageA = kBM * kBK * 4;   // 8 KiB
+constexpr uint32_t kStageA = kBM * kBK * 4;   // 8 KiB at 128 rows
 constexpr uint32_t kStageB = kBK * kBN * 4;   // 8 KiB
 constexpr size_t kSmemBytes = 1024 + kStages * (kStageA + kStageB) + 2 * kStages * sizeof(uint64_t);
 
@@ -146,16 +149,16 @@ ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
         const float* As = sA + s * (kBM * kBK);
         const float* Bs = sB + s * (kBK * kBN);
-        // Per 4 k-values: the thread's rows in two halves of 4 (i = 4h .. 4h+3),
-        // one 128-bit A read per row (4 consecutive k), two 128-bit B reads per k.
-#pragma unroll
+        // Per 4 k-values: the thread's rows in groups of kRowGroup, one 128-bit A
+        // read per row (4 consecutive k), two 128-bit B reads per k and group.
+#pragma unroll kChunkUnroll
         for (int kc = 0; kc < kBK / 4; ++kc) {
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float4 av[4];
+            for (int g = 0; g < 8 / kRowGroup; ++g) {
+                float4 av[kRowGroup];
 #pragma unroll
-                for (int ii = 0; ii < 4; ++ii) {
-                    const int i = 4 * half + ii;
+                for (int ii = 0; ii < kRowGroup; ++ii) {
+                    const int i = kRowGroup * g + ii;
                     const int r = a_row0 + 4 * i;
                     const int chunk = kc ^ (swz_even ^ ((i & 1) << 1));
                     av[ii] = *reinterpret_cast<const float4*>(As + r * kBK + chunk * 4);
@@ -168,12 +171,12 @@ ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
                                           make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
 #pragma unroll
-                    for (int ii = 0; ii < 4; ++ii) {
+                    for (int ii = 0; ii < kRowGroup; ++ii) {
                         const float a = kk == 0 ? av[ii].x : kk == 1 ? av[ii].y : kk == 2 ? av[ii].z : av[ii].w;
                         const float2 aa = make_float2(a, a);
 #pragma unroll
                         for (int p = 0; p < 4; ++p)
-                            acc[4 * half + ii][p] = __ffma2_rn(aa, bp[p], acc[4 * half + ii][p]);
+                            acc[kRowGroup * g + ii][p] = __ffma2_rn(aa, bp[p], acc[kRowGroup * g + ii][p]);
                     }
                 }
             }

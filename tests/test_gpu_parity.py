@@ -51,6 +51,18 @@ def test_edge_tiles(mode, shape):
                       f"{mode} uniform {shape}")
 
 
+# k >= 3072 takes the 256 x 256 tensor-core tiles; ragged m, n and k there too.
+WIDE_SHAPES = [(300, 520, 3100), (257, 300, 4097), (129, 1000, 3072)]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", WIDE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_long_k_tiles(mode, shape):
+    m, n, k = shape
+    parity.full_check(mode, inputs.random_case(5000 + m + n + k, m, n, k, kind="int"), f"{mode} int {shape}")
+    parity.full_check(mode, inputs.random_case(6000 + m + n + k, m, n, k, kind="uniform"), f"{mode} uniform {shape}")
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_irregular_4097x3001x1023(mode):
     # lda = 1023 and ldb = ldc = 3001: no row pitch is a multiple of 16 bytes.
