@@ -44,7 +44,7 @@ namespace {
 constexpr int kWarpRows = 4;             // warps stacked along M, each 32 rows x 64 columns
 constexpr int kBM = 32 * kWarpRows;
 constexpr int kBN = 128;
-constexpr int kBK = 16;
+constexpr int kBK = 16;                  // 16 (64-byte A rows, 64-byte swizzle) or 32 (128-byte, 128-byte swizzle)
 constexpr int kStages = 4;
 constexpr int kThreads = 64 * kWarpRows;
 constexpr int kWarps = kThreads / 32;
@@ -117,7 +117,9 @@ ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int b_col0 = 64 * wn + 4 * tn;
     // 64-byte swizzle: 16-byte chunk c of tile row r sits at chunk c ^ ((r >> 1) & 3).
     // For r = a_row0 + 4i this is (tm >> 1) ^ (2 * (i & 1)).
-    const int swz_even = tm >> 1;
+    // 128-byte swizzle (kBK = 32): chunk c of tile row r sits at c ^ (r & 7),
+    // which for r = a_row0 + 4i is tm ^ (4 * (i & 1)).
+    const int swz_even = kBK == 16 ? (tm >> 1) : tm;
 
     // acc[i][p]: row a_row0 + 4i, columns b_col0 + 2p, +1 (p < 2) and
     // b_col0 + 32 + 2(p-2), +1 (p >= 2).  Pairs of columns are updated by one
@@ -160,7 +162,7 @@ ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 for (int ii = 0; ii < kRowGroup; ++ii) {
                     const int i = kRowGroup * g + ii;
                     const int r = a_row0 + 4 * i;
-                    const int chunk = kc ^ (swz_even ^ ((i & 1) << 1));
+                    const int chunk = kc ^ (swz_even ^ ((i & 1) << (kBK == 16 ? 1 : 2)));
                     av[ii] = *reinterpret_cast<const float4*>(As + r * kBK + chunk * 4);
                 }
 #pragma unroll
@@ -213,7 +215,7 @@ ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 cudaError_t launch_ffma_f32(const Problem& p, const Device& dev) {
     CUtensorMap ta, tb;
     if (!make_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.A, p.m, p.k, p.lda, kBM, kBK,
-                         CU_TENSOR_MAP_SWIZZLE_64B) ||
+                         kBK == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.k, p.n, p.ldb, kBK, kBN,
                          CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;

@@ -35,52 +35,70 @@ constexpr int kBK = 64;                     // k per stage (128 bytes of bf16)
 constexpr int kUK = 16;                     // k per MMA
 constexpr int kTileN = 128;                 // columns of C per CTA (tensor-core M)
 constexpr uint32_t kChunkBytes = kBK * 128; // one 64-column box of B: 64 k-rows x 128 bytes
-constexpr uint32_t kStageB = 2 * kChunkBytes;
+// 128-column sub-tiles of C per CTA: each k-phase runs one MMA per sub-tile,
+// all sharing the A^T operand; wider CTAs read longer contiguous row segments
+// of B and need fewer clusters.
+constexpr int kSubTiles = 1;
 constexpr int kMaxSplit = 8;
 // k is split until about 5/3 CTAs per SM stream B (measured best on GB300
 // for 32..128 column tiles: 8 splits of 32 tiles, 4 of 64, 2 of 128).
 constexpr int kTargetCtasPer3Sms = 5;
 
-template <int NM>
+template <int NM, int NT>
 struct SkinnyCfg {
+    static constexpr uint32_t STAGE_B = NT * 2 * kChunkBytes;           // NT x 128 columns x 64 k
     static constexpr uint32_t STAGE_A = NM * 128;                       // NM rows x 64 bf16
+    static constexpr int COLS = NM < 32 ? 32 : NM;                      // TMEM columns per sub-tile
     // 4 stages keep the CTA at ~75 KiB of shared memory; measured on GB300,
     // deeper rings (8-12 stages, one CTA per SM) stream B more slowly overall.
     static constexpr int STAGES = 4;
-    static constexpr uint32_t TMEM_COLS = NM < 32 ? 32 : NM;
+    static constexpr uint32_t TMEM_COLS = NT * COLS <= 32 ? 32 : NT * COLS <= 64 ? 64 : NT * COLS <= 128 ? 128 : 256;
     static constexpr uint32_t IDESC = instr_desc(kFormatBF16, 1, 0, kTileN, NM);
-    static constexpr size_t SMEM = 1024 + STAGES * (kStageB + STAGE_A) + (2 * STAGES + 1) * 8 + 16;
-    static_assert(NM * kTileN * 4 <= STAGES * kStageB, "partial sums must fit in the B stages");
+    static constexpr size_t SMEM = 1024 + STAGES * (STAGE_B + STAGE_A) + (2 * STAGES + 1) * 8 + 16;
+    static_assert(NT * NM * kTileN * 4 <= STAGES * STAGE_B, "partial sums must fit in the B stages");
 };
 
-template <int NM>
+template <int NM, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
 umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    float* __restrict__ C, int64_t ldc, int M, int N, int K, int kb_per_split,
                    uint32_t* status) {
-    using G = SkinnyCfg<NM>;
+    using G = SkinnyCfg<NM, NT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint8_t* sB = smem;                                   // STAGES x 16 KiB
-    uint8_t* sA = smem + G::STAGES * kStageB;               // STAGES x NM*128 B
+    uint8_t* sA = smem + G::STAGES * G::STAGE_B;            // STAGES x NM*128 B
     uint64_t* full = reinterpret_cast<uint64_t*>(sA + G::STAGES * G::STAGE_A);
     uint64_t* empty = full + G::STAGES;
     uint64_t* done = empty + G::STAGES;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
-    // After the k loop the B stages hold this CTA's partial sums: red[m][j], j < 128.
+    // After the k loop the B stages hold this CTA's partial sums:
+    // red[t][m][j], sub-tile t, row m of C, column n0 + 128t + j.
     float* red = reinterpret_cast<float*>(sB);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_cta_rank();
     const uint32_t splits = gridDim.y;
-    const int n0 = blockIdx.x * kTileN;
+    const int n0 = blockIdx.x * kTileN * NT;
     const int KT = (K + kBK - 1) / kBK;
     const int kb0 = static_cast<int>(rank) * kb_per_split;
     const int kb1 = min(KT, kb0 + kb_per_split);
     const int nkb = kb1 > kb0 ? kb1 - kb0 : 0;
 
+    // The first ring's worth of loads goes out as soon as the barriers exist,
+    // so their HBM latency overlaps the tensor-memory allocation (warp 1) and
+    // the block barrier.
+    const int prefill = nkb < G::STAGES ? nkb : G::STAGES;
+    auto issue = [&](int slot, int kb) {
+        mbar_arrive_expect_tx(&full[slot], G::STAGE_B + G::STAGE_A);
+        uint8_t* b_dst = sB + slot * G::STAGE_B;
+#pragma unroll
+        for (int c = 0; c < 2 * NT; ++c)
+            tma_load_2d(b_dst + c * kChunkBytes, &tmB, &full[slot], n0 + 64 * c, kb * kBK);
+        tma_load_2d(sA + slot * G::STAGE_A, &tmA, &full[slot], kb * kBK, 0);
+    };
     if (threadIdx.x == 0) {
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
@@ -90,8 +108,9 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         }
         mbar_init(done, 1);
         fence_barrier_init();
+        for (int i = 0; i < prefill; ++i) issue(i, kb0 + i);   // empty slots: no wait needed
     }
-    if (warp == 0) tmem_alloc(tmem_slot, G::TMEM_COLS);
+    if (warp == 1) tmem_alloc(tmem_slot, G::TMEM_COLS);
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
@@ -100,15 +119,11 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     bool ok = true;
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------- TMA producer --
-        int s = 0;
-        uint32_t ph = 0;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        int s = prefill % G::STAGES;
+        uint32_t ph = prefill == G::STAGES ? 1u : 0u;
+        for (int kb = kb0 + prefill; kb < kb1; ++kb) {
             if (!mbar_wait(&empty[s], ph ^ 1u, status)) { ok = false; break; }
-            mbar_arrive_expect_tx(&full[s], kStageB + G::STAGE_A);
-            uint8_t* b_dst = sB + s * kStageB;
-            tma_load_2d(b_dst, &tmB, &full[s], n0, kb * kBK);
-            tma_load_2d(b_dst + kChunkBytes, &tmB, &full[s], n0 + 64, kb * kBK);
-            tma_load_2d(sA + s * G::STAGE_A, &tmA, &full[s], kb * kBK, 0);
+            issue(s, kb);
             if (++s == G::STAGES) { s = 0; ph ^= 1u; }
         }
     } else if (warp == 1 && lane == 0) {
@@ -118,16 +133,20 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         for (int i = 0; i < nkb; ++i) {
             if (!mbar_wait(&full[s], ph, status)) { ok = false; break; }
             tc_fence_after_sync();
-            const uint32_t b0 = smem_addr(sB + s * kStageB);
+            const uint32_t b0 = smem_addr(sB + s * G::STAGE_B);
             const uint32_t a0 = smem_addr(sA + s * G::STAGE_A);
 #pragma unroll
             for (int kk = 0; kk < kBK / kUK; ++kk) {
-                // tensor-core A = B^T: MN-major, 64-column chunks kChunkBytes apart,
-                // 8-row k groups 1 KiB apart; slice kk starts kUK rows down.
-                const uint64_t ad = smem_desc(b0 + kk * kUK * 128, kChunkBytes, 1024, kSwizzle128B);
                 // tensor-core B = A^T: K-major rows of 128 bytes, 8-row groups 1 KiB apart.
                 const uint64_t bd = smem_desc(a0 + kk * 32, 16, 1024, kSwizzle128B);
-                umma_f16(tmem, ad, bd, G::IDESC, (i | kk) != 0);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    // tensor-core A = B^T of sub-tile t: MN-major, 64-column chunks
+                    // kChunkBytes apart, 8-row k groups 1 KiB apart; slice kk starts kUK rows down.
+                    const uint64_t ad =
+                        smem_desc(b0 + t * 2 * kChunkBytes + kk * kUK * 128, kChunkBytes, 1024, kSwizzle128B);
+                    umma_f16(tmem + t * G::COLS, ad, bd, G::IDESC, (i | kk) != 0);
+                }
             }
             umma_commit(&empty[s]);
             if (++s == G::STAGES) { s = 0; ph ^= 1u; }
@@ -141,21 +160,27 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     if (have && !mbar_wait(done, 0, status)) have = false;
     tc_fence_after_sync();
     __syncwarp();   // tcgen05.ld is warp-collective
-    const int jrow = warp * 32 + lane;   // tensor-memory lane = column n0 + jrow of C
-    if (NM == 16) {
-        uint32_t r[16];
-        tmem_load_16(tmem + (static_cast<uint32_t>(warp * 32) << 16), r);
-        tmem_load_wait();
+    const int jrow = warp * 32 + lane;   // tensor-memory lane = column n0 + 128t + jrow of C
 #pragma unroll
-        for (int j = 0; j < 16; ++j) red[j * kTileN + jrow] = have ? __uint_as_float(r[j]) : 0.0f;
-    } else {
-#pragma unroll
-        for (int c = 0; c < NM / 32; ++c) {
-            uint32_t r[32];
-            tmem_load_32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c * 32, r);
+    for (int t = 0; t < NT; ++t) {
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + t * G::COLS;
+        float* red_t = red + t * NM * kTileN;
+        if (NM == 16) {
+            uint32_t r[16];
+            tmem_load_16(taddr, r);
             tmem_load_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) red[(c * 32 + j) * kTileN + jrow] = have ? __uint_as_float(r[j]) : 0.0f;
+            for (int j = 0; j < 16; ++j) red_t[j * kTileN + jrow] = have ? __uint_as_float(r[j]) : 0.0f;
+        } else {
+#pragma unroll
+            for (int c = 0; c < NM / 32; ++c) {
+                uint32_t r[32];
+                tmem_load_32(taddr + c * 32, r);
+                tmem_load_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    red_t[(c * 32 + j) * kTileN + jrow] = have ? __uint_as_float(r[j]) : 0.0f;
+            }
         }
     }
     tc_fence_before_sync();
@@ -164,10 +189,12 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
     // --------------------------- add the S partials in rank order, store --
     const int rows = M < NM ? M : NM;
-    const int n = n0 + static_cast<int>(threadIdx.x);
     const uint32_t my_red = smem_addr(red);
-    for (int mr = static_cast<int>(rank); mr < rows; mr += static_cast<int>(splits)) {
-        const uint32_t off = static_cast<uint32_t>((mr * kTileN + static_cast<int>(threadIdx.x)) * 4);
+    for (int item = static_cast<int>(rank); item < NT * rows; item += static_cast<int>(splits)) {
+        const int t = item / rows, mr = item - t * rows;
+        const int n = n0 + t * kTileN + static_cast<int>(threadIdx.x);
+        const uint32_t off =
+            static_cast<uint32_t>(((t * NM + mr) * kTileN + static_cast<int>(threadIdx.x)) * 4);
         float sum = 0.0f;
         for (uint32_t q = 0; q < splits; ++q) sum += ld_cluster_f32(cluster_map(my_red + off, q));
         if (n < N) C[static_cast<int64_t>(mr) * ldc + n] = sum;
@@ -175,7 +202,7 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     __syncwarp();
     cluster_sync_all();   // partials stay readable until every CTA is done with them
 
-    if (warp == 0) {
+    if (warp == 1) {   // the allocating warp frees the tensor memory
         __syncwarp();
         tc_fence_after_sync();
         tmem_dealloc(tmem, G::TMEM_COLS);
@@ -185,21 +212,22 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
 template <int NM>
 cudaError_t launch_nm(const Problem& p, const Device& dev) {
-    using G = SkinnyCfg<NM>;
+    constexpr int NT = kSubTiles;
+    using G = SkinnyCfg<NM, NT>;
     CUtensorMap ta, tb;
     if (!make_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.A, p.m, p.k, p.lda, NM, kBK,
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.B, p.k, p.n, p.ldb, kBK, 64,
                          CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    auto kernel = umma_skinny_kernel<NM>;
+    auto kernel = umma_skinny_kernel<NM, NT>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(G::SMEM));
     if (err != cudaSuccess) {
         set_error("cudaFuncSetAttribute(umma_skinny_kernel): %s", cudaGetErrorString(err));
         return err;
     }
-    const int tiles = (p.n + kTileN - 1) / kTileN;
+    const int tiles = (p.n + kTileN * NT - 1) / (kTileN * NT);
     const int KT = (p.k + kBK - 1) / kBK;
     const int target = kTargetCtasPer3Sms * dev.sm_count / 3;
     int splits = (target + tiles / 2) / tiles;
