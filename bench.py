@@ -342,6 +342,40 @@ def bench_tgemm(args, world, rank, local):
     roof["kernel"] = KERNEL_NAMES[PARTS[dominant][1]]
     roof["workload"] = dominant
 
+    # The lecture's transpose case study (naive -> coalesced shared tile ->
+    # padded tile) next to libtgemm's transpose, at the lecture's 1024 x 1024
+    # and at 16384 x 16384 (HBM-bound); GB/s counts the bytes read and written.
+    transposes = {}
+    if not args.no_extras:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(1006)
+        kernels = {"tgemm_transpose_f32": lambda a, b: tgemm.tgemm_transpose_f32(a, b, stream),
+                   "pages_naive": lambda a, b: pages.tgemm_pages_transpose_f32(a, b, "naive", stream),
+                   "pages_coalesced": lambda a, b: pages.tgemm_pages_transpose_f32(a, b, "coalesced", stream),
+                   "pages_padded": lambda a, b: pages.tgemm_pages_transpose_f32(a, b, "padded", stream)}
+        for rows, cols in [(1024, 1024), (16384, 16384)]:
+            nbytes = rows * cols * 4
+            R = max(1, -(-rotate_bytes // nbytes))
+            srcs = [torch.empty((rows, cols), device=dev).normal_(generator=gen) for _ in range(R)]
+            dst = torch.empty((cols, rows), device=dev)
+            for name, fn in kernels.items():
+                ev = []
+                for it in range(args.warmup + 10):
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fn(srcs[it % R], dst)
+                    e1.record(stream)
+                    ev.append((e0, e1))
+                torch.cuda.synchronize(dev)
+                ts = [a.elapsed_time(b) / 1e3 for a, b in ev[args.warmup:]]
+                avg = sum(ts) / len(ts)
+                gbs = 2 * nbytes / avg / 1e9
+                transposes[f"{name}_{rows}x{cols}"] = {
+                    "us": round(avg * 1e6, 2), "GB_s": round(gbs, 1),
+                    "frac_of_hbm": round(gbs / float(peaks["hbm_gbs"]), 4)}
+            del srcs, dst
+
     # End to end through the C ABI: pinned host inputs -> device, product, result -> host.
     e2e = None
     if not args.no_e2e:
@@ -400,7 +434,7 @@ def bench_tgemm(args, world, rank, local):
                 "config": {"workload": "gemm 8192x8192x8192 bf16->fp32 (tcgen05) + 4096x4096x4096 fp32 (FFMA)",
                            "l2": "inputs larger than L2: each launch reads the next of R input copies (>= 384 MiB per shape)",
                            "parallelism": f"replicas x{world}"},
-                "roofline": roof, "parts": parts, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roof, "parts": parts, "transposes": transposes, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": int(launches), "clocks": clocks.summary(),
                 "wall_s_timed_region": round(t_wall, 3), "impl": "tgemm"}
         print(json.dumps(line), flush=True)

@@ -353,6 +353,43 @@ tgemm_status tgemm_bf16(int64_t m, int64_t n, int64_t k, const void* A, int64_t 
     return tgemm::run(tgemm::Kind::BF16, m, n, k, A, lda, B, ldb, C, ldc, stream);
 }
 
+tgemm_status tgemm_transpose_f32(int64_t rows, int64_t cols, const float* src, int64_t ld_src, float* dst,
+                                 int64_t ld_dst, struct CUstream_st* stream) {
+    using namespace tgemm;
+    clear_error();
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (rows < 0 || cols < 0 || rows > lim || cols > lim) {
+        set_error("sizes must satisfy 0 <= rows, cols < 2^31");
+        return TGEMM_ERR_INVALID_VALUE;
+    }
+    if (rows == 0 || cols == 0) return TGEMM_OK;
+    if (ld_src < cols || ld_dst < rows || ld_src > (int64_t(1) << 40) || ld_dst > (int64_t(1) << 40)) {
+        set_error("leading dimensions must satisfy ld_src >= cols and ld_dst >= rows");
+        return TGEMM_ERR_INVALID_VALUE;
+    }
+    if (!src || !dst) {
+        set_error("NULL pointer for a matrix with nonzero extent");
+        return TGEMM_ERR_INVALID_VALUE;
+    }
+    if (reinterpret_cast<uintptr_t>(src) % 4 || reinterpret_cast<uintptr_t>(dst) % 4) {
+        set_error("pointers must be aligned to 4 bytes");
+        return TGEMM_ERR_INVALID_VALUE;
+    }
+    const uint64_t s_bytes = span_bytes(rows, cols, ld_src, 4);
+    const uint64_t d_bytes = span_bytes(cols, rows, ld_dst, 4);
+    if (overlaps(src, s_bytes, dst, d_bytes)) {
+        set_error("dst overlaps src");
+        return TGEMM_ERR_INVALID_VALUE;
+    }
+    Device* dev = nullptr;
+    tgemm_status st = current_device(&dev);
+    if (st != TGEMM_OK) return st;
+    if ((st = check_span("src", src, s_bytes, dev->ordinal)) != TGEMM_OK) return st;
+    if ((st = check_span("dst", dst, d_bytes, dev->ordinal)) != TGEMM_OK) return st;
+    return launch_transpose(src, ld_src, dst, ld_dst, rows, cols, stream, *dev) == cudaSuccess ? TGEMM_OK
+                                                                                               : TGEMM_ERR_CUDA;
+}
+
 const char* tgemm_status_string(tgemm_status status) {
     switch (status) {
         case TGEMM_OK: return "success";

@@ -49,6 +49,40 @@ __global__ void tiled_kernel(const float* __restrict__ M, int64_t ldm, const flo
     if (row < rows && col < cols) P[static_cast<int64_t>(row) * ldp + col] = pvalue;
 }
 
+// Transposes of the lecture's case study: TILE x TILE tiles, TILE x 8 threads,
+// each thread moving 4 elements (rows ty, ty+8, ty+16, ty+24 of the tile).
+constexpr int kTT = 32;
+constexpr int kTR = 8;
+
+// Naive: read row-wise (coalesced), write column-wise (strided, uncoalesced).
+__global__ void transpose_naive_kernel(const float* __restrict__ in, int64_t ld_in, float* __restrict__ out,
+                                       int64_t ld_out, int rows, int cols) {
+    const int x = blockIdx.x * kTT + threadIdx.x;   // input column
+    const int y0 = blockIdx.y * kTT + threadIdx.y;  // input row
+    for (int j = 0; j < kTT; j += kTR) {
+        const int y = y0 + j;
+        if (x < cols && y < rows) out[static_cast<int64_t>(x) * ld_out + y] = in[static_cast<int64_t>(y) * ld_in + x];
+    }
+}
+
+// Shared-memory tile: coalesced read into the tile, barrier, block offsets
+// swapped, a column of the tile written out coalesced.  PAD = 0 is tile[32][32]
+// (a warp reading a column hits one bank 32 times), PAD = 1 is tile[32][33].
+template <int PAD>
+__global__ void transpose_tiled_kernel(const float* __restrict__ in, int64_t ld_in, float* __restrict__ out,
+                                       int64_t ld_out, int rows, int cols) {
+    __shared__ float tile[kTT][kTT + PAD];
+    int x = blockIdx.x * kTT + threadIdx.x;
+    int y = blockIdx.y * kTT + threadIdx.y;
+    for (int j = 0; j < kTT; j += kTR)
+        if (x < cols && y + j < rows) tile[threadIdx.y + j][threadIdx.x] = in[static_cast<int64_t>(y + j) * ld_in + x];
+    __syncthreads();
+    x = blockIdx.y * kTT + threadIdx.x;   // output column = input row
+    y = blockIdx.x * kTT + threadIdx.y;   // output row = input column
+    for (int j = 0; j < kTT; j += kTR)
+        if (x < rows && y + j < cols) out[static_cast<int64_t>(y + j) * ld_out + x] = tile[threadIdx.x][threadIdx.y + j];
+}
+
 using AddressRangeFn = CUresult (*)(CUdeviceptr*, size_t*, CUdeviceptr);
 
 AddressRangeFn address_range() {
@@ -138,5 +172,34 @@ extern "C" int tgemm_pages_tiled_f32(int64_t m, int64_t n, int64_t k, const floa
     else
         tiled_kernel<32><<<grid, block, 0, stream>>>(A, lda, B, ldb, C, ldc, static_cast<int>(m),
                                                       static_cast<int>(n), static_cast<int>(k));
+    return cudaGetLastError() == cudaSuccess ? TGEMM_OK : TGEMM_ERR_CUDA;
+}
+
+extern "C" int tgemm_pages_transpose_f32(int64_t rows, int64_t cols, const float* src, int64_t ld_src, float* dst,
+                                         int64_t ld_dst, int variant, struct CUstream_st* stream) {
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (variant < 0 || variant > 2 || rows < 0 || cols < 0 || rows > lim || cols > lim) return TGEMM_ERR_INVALID_VALUE;
+    if (rows == 0 || cols == 0) return TGEMM_OK;
+    if (ld_src < cols || ld_dst < rows || !src || !dst) return TGEMM_ERR_INVALID_VALUE;
+    const uint64_t sb = span(rows, cols, ld_src), db = span(cols, rows, ld_dst);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src), b = reinterpret_cast<uintptr_t>(dst);
+    if (a < b + db && b < a + sb) return TGEMM_ERR_INVALID_VALUE;
+    if (!span_ok(src, sb) || !span_ok(dst, db)) return TGEMM_ERR_INVALID_VALUE;
+    int dev = -1, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return TGEMM_ERR_CUDA;
+    if (major != 10 || minor != 3) return TGEMM_ERR_UNSUPPORTED_DEVICE;
+    const dim3 block(kTT, kTR);
+    const dim3 grid(static_cast<unsigned>((cols + kTT - 1) / kTT), static_cast<unsigned>((rows + kTT - 1) / kTT));
+    if (grid.y > 65535) return TGEMM_ERR_INVALID_VALUE;
+    const int r = static_cast<int>(rows), c = static_cast<int>(cols);
+    if (variant == 0)
+        transpose_naive_kernel<<<grid, block, 0, stream>>>(src, ld_src, dst, ld_dst, r, c);
+    else if (variant == 1)
+        transpose_tiled_kernel<0><<<grid, block, 0, stream>>>(src, ld_src, dst, ld_dst, r, c);
+    else
+        transpose_tiled_kernel<1><<<grid, block, 0, stream>>>(src, ld_src, dst, ld_dst, r, c);
     return cudaGetLastError() == cudaSuccess ? TGEMM_OK : TGEMM_ERR_CUDA;
 }

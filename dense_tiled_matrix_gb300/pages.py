@@ -15,6 +15,7 @@ SIGNATURES = {
     "tgemm_pages_naive_f32": (ctypes.c_int, [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, _VP]),
     "tgemm_pages_tiled_f32": (ctypes.c_int, [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, ctypes.c_int,
                                              _VP]),
+    "tgemm_pages_transpose_f32": (ctypes.c_int, [_I64, _I64, _VP, _I64, _VP, _I64, ctypes.c_int, _VP]),
 }
 
 _lock = threading.Lock()
@@ -64,3 +65,17 @@ def tgemm_pages_tiled_f32(A, B, C=None, tile_width=16, stream=None):
     _check(load().tgemm_pages_tiled_f32(m, n, k, A.data_ptr() or None, _t._ld(A), B.data_ptr() or None, _t._ld(B),
                                         C.data_ptr() or None, _t._ld(C), int(tile_width), _t._stream_handle(stream)))
     return C
+
+
+TRANSPOSE_VARIANTS = {"naive": 0, "coalesced": 1, "padded": 2}
+
+
+def tgemm_pages_transpose_f32(src, dst=None, variant="padded", stream=None):
+    """The lecture's transpose kernels: variant "naive", "coalesced" (tile[32][32]) or "padded" (tile[32][33])."""
+    import torch
+    rows, cols = int(src.shape[0]), int(src.shape[1])
+    if dst is None:
+        dst = torch.empty((cols, rows), dtype=torch.float32, device=src.device)
+    _check(load().tgemm_pages_transpose_f32(rows, cols, src.data_ptr() or None, _t._ld(src), dst.data_ptr() or None,
+                                            _t._ld(dst), TRANSPOSE_VARIANTS[variant], _t._stream_handle(stream)))
+    return dst

@@ -32,6 +32,7 @@ SIGNATURES = {
     "tgemm_tf32": (ctypes.c_int, _GEMM_ARGS),
     "tgemm_bf16": (ctypes.c_int, _GEMM_ARGS),
     "tgemm_tf32_noalloc": (ctypes.c_int, _GEMM_ARGS),
+    "tgemm_transpose_f32": (ctypes.c_int, [_I64, _I64, _VP, _I64, _VP, _I64, _VP]),
     "tgemm_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "tgemm_last_error": (ctypes.c_char_p, []),
     "tgemm_get_device_status": (ctypes.c_int, [_VP]),
@@ -136,6 +137,21 @@ def tgemm_tf32_noalloc(A, B, C=None, stream=None):
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def tgemm_transpose_f32(src, dst=None, stream=None):
+    """dst = src.T for a float32 CUDA matrix (row-major views with any pitch)."""
+    import torch
+    if src.dtype != torch.float32 or src.dim() != 2:
+        raise TypeError("tgemm_transpose_f32: src must be a 2-D float32 tensor")
+    rows, cols = int(src.shape[0]), int(src.shape[1])
+    if dst is None:
+        dst = torch.empty((cols, rows), dtype=torch.float32, device=src.device)
+    if dst.dtype != torch.float32 or tuple(dst.shape) != (cols, rows):
+        raise ValueError(f"tgemm_transpose_f32: dst must be float32 of shape ({cols}, {rows})")
+    _check(load().tgemm_transpose_f32(rows, cols, src.data_ptr() or None, _ld(src), dst.data_ptr() or None,
+                                      _ld(dst), _stream_handle(stream)))
+    return dst
 
 
 def tgemm_status_string(status: int) -> str:

@@ -108,6 +108,20 @@ tgemm_status tgemm_bf16(int64_t m, int64_t n, int64_t k,
                         float *C, int64_t ldc,
                         struct CUstream_st *stream);
 
+/* dst = transpose of src: dst[j*ld_dst + i] = src[i*ld_src + j] for
+ * 0 <= i < rows, 0 <= j < cols; 4-byte elements (fp32), device pointers.
+ * note.jhbae.stream "Lec 29 · GPU Architecture (2)", matrix transpose case
+ * study: tiles read with coalesced row accesses into shared memory padded by
+ * one word per row, columns written back coalesced; with 16-byte aligned
+ * matrices and pitches (ld % 4 == 0) every access is 128 bits wide.  This is
+ * the kernel that gives tgemm_tf32 its k-contiguous copy of B.  Rules: rows,
+ * cols >= 0 and < 2^31, ld_src >= cols, ld_dst >= rows, dst must not overlap
+ * src; rows == 0 or cols == 0 is a no-op. */
+tgemm_status tgemm_transpose_f32(int64_t rows, int64_t cols,
+                                 const float *src, int64_t ld_src,
+                                 float *dst, int64_t ld_dst,
+                                 struct CUstream_st *stream);
+
 /* Size of the static device array used by tgemm_tf32_noalloc (32 MiB). */
 #define TGEMM_NOALLOC_SCRATCH_BYTES (32ull << 20)
 

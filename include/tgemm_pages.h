@@ -23,6 +23,14 @@
  *    multiples of the tile read zeros outside M and N and store nothing
  *    outside C.
  *
+ * tgemm_pages_transpose_f32 is the matrix-transpose case study of note.jhbae.stream
+ * "Lec 29 · GPU Architecture (2)": dst[j*ld_dst + i] = src[i*ld_src + j] with
+ * 32 x 32 tiles and 32 x 8 threads, 4 elements per thread.  variant 0 reads
+ * rows and writes columns straight from global memory (uncoalesced writes);
+ * variant 1 goes through a shared tile[32][32] and writes coalesced (a column
+ * read of the tile is a 32-way bank conflict); variant 2 pads the tile to
+ * [32][33], which removes the conflicts.
+ *
  * Arguments, ownership and status codes are those of tgemm.h (device
  * pointers owned by the caller, asynchronous on `stream`).  The status values
  * are the tgemm_status codes.
@@ -50,6 +58,12 @@ int tgemm_pages_tiled_f32(int64_t m, int64_t n, int64_t k,
                           float *C, int64_t ldc,
                           int tile_width,
                           struct CUstream_st *stream);
+
+int tgemm_pages_transpose_f32(int64_t rows, int64_t cols,
+                              const float *src, int64_t ld_src,
+                              float *dst, int64_t ld_dst,
+                              int variant,
+                              struct CUstream_st *stream);
 
 #ifdef __cplusplus
 }

@@ -16,8 +16,10 @@ Contents
                  Block(0,0) and "Memory 분석"), used to pin the oracle and the
                  load-count model on small cases.
 
-Every function returns fp64 results: P(i,j) = sum_k M(i,k) N(k,j) and the
-error scale D(i,j) = sum_k |M(i,k)| |N(k,j)|.
+The products return fp64 results: P(i,j) = sum_k M(i,k) N(k,j) and the error
+scale D(i,j) = sum_k |M(i,k)| |N(k,j)|.  ``transpose`` is the plain definition
+T(j,i) = M(i,j) of the lecture's transpose case study (note.jhbae.stream
+"Lec 29 · GPU Architecture (2)"), used to check the transpose kernels.
 """
 from __future__ import annotations
 
@@ -159,3 +161,11 @@ def gemm_entries(M: np.ndarray, N: np.ndarray, rows, cols, lib=None):
     if rc != 0:
         raise RuntimeError(f"oracle_gemm_entries failed with code {rc}")
     return P, D
+
+
+def transpose(M: np.ndarray) -> np.ndarray:
+    """T with T[j, i] = M[i, j] (numpy's transpose, materialised), same dtype."""
+    M = np.asarray(M)
+    if M.ndim != 2:
+        raise ValueError("oracle: transpose takes a 2-D array")
+    return np.ascontiguousarray(M.T)

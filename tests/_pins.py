@@ -254,9 +254,20 @@ def pin_tiled_walk(lib):
         assert np.array_equal(P, np.array(Pt, dtype=np.float64)), f"tiled walk {m}x{n}x{k} T={T}"
 
 
+def pin_transpose(lib):
+    # element (i, j) of a 5 x 3 matrix holds 10 i + j: after transposing, element
+    # (j, i) must hold 10 i + j; transposing twice is the identity.
+    M = np.array([[10 * i + j for j in range(3)] for i in range(5)], dtype=np.float32)
+    T = oracle.transpose(M)
+    assert T.shape == (3, 5)
+    assert all(T[j, i] == 10 * i + j for i in range(5) for j in range(3)), "transpose element map"
+    assert np.array_equal(oracle.transpose(T), M), "transpose twice"
+    assert oracle.transpose(np.zeros((0, 4))).shape == (4, 0)
+
+
 PINS = [pin_worked_example, pin_identity, pin_permutation, pin_all_ones, pin_rank1,
         pin_alternating_signs, pin_brute_force, pin_numpy, pin_dtypes,
-        pin_entries_match_full, pin_threads, pin_leading_dims, pin_empty, pin_tiled_walk]
+        pin_entries_match_full, pin_threads, pin_leading_dims, pin_empty, pin_tiled_walk, pin_transpose]
 
 
 def failing_pins(lib):
