@@ -41,19 +41,27 @@
 namespace tgemm {
 namespace {
 
-constexpr int kWarpRows = 4;             // warps stacked along M, each 32 rows x 64 columns
-constexpr int kBM = 32 * kWarpRows;
 constexpr int kBN = 128;
 constexpr int kBK = 16;                  // 16 (64-byte A rows, 64-byte swizzle) or 32 (128-byte, 128-byte swizzle)
 constexpr int kStages = 4;
-constexpr int kThreads = 64 * kWarpRows;
-constexpr int kWarps = kThreads / 32;
 constexpr int kRowGroup = 4;             // rows of a thread processed together (4 or 8)
 constexpr int kChunkUnroll = 4;          // unrolling of the 4-wide k chunks of a stage (1..4)
 constexpr int kGroupM = 8;
-constexpr uint32_t kStageA = kBM * kBK * 4;   // 8 KiB at 128 rows
 constexpr uint32_t kStageB = kBK * kBN * 4;   // 8 KiB
-constexpr size_t kSmemBytes = 1024 + kStages * (kStageA + kStageB) + 2 * kStages * sizeof(uint64_t);
+
+// WR warps stacked along M (each warp 32 rows x 64 columns, two warps across
+// N): WR = 4 gives 128 x 128 tiles and one 256-thread CTA per SM; WR = 2 gives
+// 64 x 128 tiles and two 128-thread CTAs per SM, whose barrier and prologue
+// waits overlap each other (better when k is short).
+template <int WR>
+struct FCfg {
+    static constexpr int BM = 32 * WR;
+    static constexpr int THREADS = 64 * WR;
+    static constexpr int WARPS = THREADS / 32;
+    static constexpr int MIN_BLOCKS = WR == 2 ? 2 : 1;
+    static constexpr uint32_t STAGE_A = BM * kBK * 4;   // 8 KiB at 128 rows
+    static constexpr size_t SMEM = 1024 + kStages * (STAGE_A + kStageB) + 2 * kStages * sizeof(uint64_t);
+};
 
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int& tm, int& tn) {
     const int per_group = kGroupM * tiles_n;
@@ -65,10 +73,15 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
     tn = in_group / rows;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int WR>
+__global__ void __launch_bounds__(FCfg<WR>::THREADS, FCfg<WR>::MIN_BLOCKS)
 ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 float* __restrict__ C, int64_t ldc, int M, int N, int K, int vec_store,
                 uint32_t* status) {
+    using F = FCfg<WR>;
+    constexpr int kBM = F::BM;
+    constexpr int kWarps = F::WARPS;
+    constexpr uint32_t kStageA = F::STAGE_A;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -210,29 +223,40 @@ ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
 }
 
-}  // namespace
-
-cudaError_t launch_ffma_f32(const Problem& p, const Device& dev) {
+template <int WR>
+cudaError_t launch_wr(const Problem& p, const Device& dev) {
+    using F = FCfg<WR>;
     CUtensorMap ta, tb;
-    if (!make_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.A, p.m, p.k, p.lda, kBM, kBK,
+    if (!make_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.A, p.m, p.k, p.lda, F::BM, kBK,
                          kBK == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.k, p.n, p.ldb, kBK, kBN,
                          CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(ffma_f32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(kSmemBytes));
+    auto kernel = ffma_f32_kernel<WR>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(F::SMEM));
     if (err != cudaSuccess) {
         set_error("cudaFuncSetAttribute(ffma_f32_kernel): %s", cudaGetErrorString(err));
         return err;
     }
-    const int64_t tiles = static_cast<int64_t>((p.m + kBM - 1) / kBM) * ((p.n + kBN - 1) / kBN);
+    const int64_t tiles = static_cast<int64_t>((p.m + F::BM - 1) / F::BM) * ((p.n + kBN - 1) / kBN);
     const int vec_store = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
-    ffma_f32_kernel<<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, p.stream>>>(
-        ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status);
+    kernel<<<static_cast<unsigned>(tiles), F::THREADS, F::SMEM, p.stream>>>(ta, tb, p.C, p.ldc, p.m, p.n, p.k,
+                                                                            vec_store, dev.status);
     count_launch();
     err = cudaGetLastError();
     if (err != cudaSuccess) set_error("ffma_f32_kernel launch: %s", cudaGetErrorString(err));
     return err;
+}
+
+// Measured on GB300: 4096^3 53.2 TFLOP/s with 128-row CTAs vs 52.6 with two
+// 64-row CTAs per SM; 4097 x 3001 x 1024 42.8 vs 46.3.
+constexpr int kShortK = 2048;
+
+}  // namespace
+
+cudaError_t launch_ffma_f32(const Problem& p, const Device& dev) {
+    return p.k < kShortK ? launch_wr<2>(p, dev) : launch_wr<4>(p, dev);
 }
 
 }  // namespace tgemm

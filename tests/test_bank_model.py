@@ -119,9 +119,11 @@ def test_ffma_b_reads_take_one_pass(warp):
             assert wavefronts(addrs, width=16) == 1, (warp, k, half)
 
 
-def test_ffma_thread_tiles_cover_the_cta_tile_once():
+@pytest.mark.parametrize("warp_rows", [2, 4])
+def test_ffma_thread_tiles_cover_the_cta_tile_once(warp_rows):
+    # warp_rows warps stacked along M, two across N: a (32 warp_rows) x 128 tile
     seen = set()
-    for warp in range(8):
+    for warp in range(2 * warp_rows):
         for lane in range(32):
             wm, wn, tm, tn = ffma_lane(warp, lane)
             for i in range(8):
@@ -130,4 +132,4 @@ def test_ffma_thread_tiles_cover_the_cta_tile_once():
                         cell = (32 * wm + tm + 4 * i, 64 * wn + 4 * tn + 32 * h + j)
                         assert cell not in seen
                         seen.add(cell)
-    assert seen == {(r, c) for r in range(128) for c in range(128)}
+    assert seen == {(r, c) for r in range(32 * warp_rows) for c in range(128)}
