@@ -63,7 +63,15 @@ EXTRAS = {
     "pages_tiled32_4096": ("n4096", "pages_tiled32", "f32"),
 }
 SLOW_EXTRA_ITERS = 4   # timed launches of the pages' kernels (tens of ms each)
-KERNEL_NAMES = {"f32": "ffma_f32_kernel", "tf32": "umma_kernel<true>", "bf16": "umma_kernel<false>"}
+# DRAM bytes (read + write) per launch of the main kernel of a shape, from one
+# ncu capture of the current kernel (summaries under profiles/).  Must be
+# re-taken whenever that kernel changes; shapes without an entry report null.
+NCU_TRAFFIC = {
+    "f32_4096": (403.26e6, "profiles/ffma_f32_4096.md (ffma_f32_kernel<4>)"),
+    "bf16_8192": (1112.58e6, "profiles/umma_bf16_8192.md (umma_kernel<0, 0, 1>)"),
+    "tf32_4096": (264.65e6, "profiles/umma_tf32_4096.md (umma_kernel<1, 1, 1>, without the B transpose)"),
+}
+KERNEL_NAMES = {"f32": "ffma_f32_kernel<4>", "tf32": "umma_kernel<1, 1, 1>", "bf16": "umma_kernel<0, 0, 1>"}
 
 
 def load_peaks():
@@ -333,10 +341,14 @@ def bench_tgemm(args, world, rank, local):
         c = (runs.get(name) or extras.get(name))[0]
         entry = (PARTS.get(name) or EXTRAS.get(name))[1]
         avg = sum(ts) / len(ts)
+        roof_part = roofline_for(entry, c, avg, peaks, peaks_src)
+        if name in NCU_TRAFFIC:
+            roof_part["traffic"] = int(NCU_TRAFFIC[name][0])
+            roof_part["traffic_source"] = NCU_TRAFFIC[name][1]
         parts[name] = {"m": c.m, "n": c.n, "k": c.k, "entry": f"tgemm_{entry}", "launches_timed": len(ts),
                        "ms": round(avg * 1e3, 4),
                        "tflops": round(2.0 * c.m * c.n * c.k / avg / 1e12, 2),
-                       "roofline": roofline_for(entry, c, avg, peaks, peaks_src)}
+                       "roofline": roof_part}
     dominant = max(PARTS, key=lambda n: sum(per[n]))
     roof = dict(parts[dominant]["roofline"])
     roof["kernel"] = KERNEL_NAMES[PARTS[dominant][1]]
