@@ -195,8 +195,15 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         const int n = n0 + t * kTileN + static_cast<int>(threadIdx.x);
         const uint32_t off =
             static_cast<uint32_t>(((t * NM + mr) * kTileN + static_cast<int>(threadIdx.x)) * 4);
+        // all remote loads first (they overlap), then the sum in rank order
+        float part[kMaxSplit];
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q)
+            part[q] = q < static_cast<int>(splits) ? ld_cluster_f32(cluster_map(my_red + off, q)) : 0.0f;
         float sum = 0.0f;
-        for (uint32_t q = 0; q < splits; ++q) sum += ld_cluster_f32(cluster_map(my_red + off, q));
+#pragma unroll
+        for (int q = 0; q < kMaxSplit; ++q)
+            if (q < static_cast<int>(splits)) sum += part[q];
         if (n < N) C[static_cast<int64_t>(mr) * ldc + n] = sum;
     }
     __syncwarp();
