@@ -73,136 +73,85 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
     tn = in_group / rows;
 }
 
-template <int WR>
-__global__ void __launch_bounds__(FCfg<WR>::THREADS, FCfg<WR>::MIN_BLOCKS)
-ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                float* __restrict__ C, int64_t ldc, int M, int N, int K, int vec_store,
-                uint32_t* status) {
-    using F = FCfg<WR>;
-    constexpr int kBM = F::BM;
-    constexpr int kWarps = F::WARPS;
-    constexpr uint32_t kStageA = F::STAGE_A;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
-    float* sA = reinterpret_cast<float*>(smem);
-    float* sB = reinterpret_cast<float*>(smem + kStages * kStageA);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * (kStageA + kStageB));
-    uint64_t* empty = full + kStages;
+__device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
 
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    const int tiles_m = (M + kBM - 1) / kBM;
-    const int tiles_n = (N + kBN - 1) / kBN;
-    int tile_m, tile_n;
-    tile_coords(blockIdx.x, tiles_m, tiles_n, tile_m, tile_n);
-    const int m0 = tile_m * kBM;
-    const int n0 = tile_n * kBN;
-    const int KT = (K + kBK - 1) / kBK;
+__device__ __forceinline__ void st_release_u32(unsigned* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
 
-    if (tid == 0) {
-        tma_prefetch_map(&tmA);
-        tma_prefetch_map(&tmB);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kWarps);
+// Waits (bounded, like the mbarrier waits) until *flag != 0.
+__device__ bool wait_flag(const unsigned* flag, uint32_t* status) {
+    if (ld_acquire_u32(flag)) return true;
+    const uint64_t start = global_timer_ns();
+    while (!ld_acquire_u32(flag)) {
+        if (global_timer_ns() - start > kWaitLimitNs) {
+            atomicCAS(status, 0u, kStatusTimeout);
+            return false;
         }
-        fence_barrier_init();
+        __nanosleep(100);
     }
-    __syncthreads();
+    return true;
+}
 
-    if (tid == 0) {
-        const int first = KT < kStages ? KT : kStages;
-        for (int s = 0; s < first; ++s) {
-            mbar_arrive_expect_tx(&full[s], kStageA + kStageB);
-            tma_load_2d(sA + s * (kBM * kBK), &tmA, &full[s], s * kBK, m0);
-            tma_load_2d(sB + s * (kBK * kBN), &tmB, &full[s], n0, s * kBK);
-        }
-    }
+// Per-thread register tile: acc[i][p] holds row a_row0 + 4i and columns
+// b_col0 + 2p, +1 (p < 2) or b_col0 + 32 + 2(p-2), +1 (p >= 2) of the CTA
+// tile.  Pairs of columns are updated by one paired FMA (fma.rn.f32x2): each
+// lane is an ordinary fused multiply-add with one rounding, exactly as fmaf.
+using Acc = float2[8][4];
 
-    // Thread layout: warp (wm, wn) covers rows 32*wm .. +31 and columns
-    // 64*wn .. +63; lane (tm, tn) takes rows tm + 4i (i < 8) and columns
-    // 4*tn .. +3 and 32 + 4*tn .. +3 of that warp tile.
-    const int wm = warp >> 1, wn = warp & 1;
-    const int tm = lane >> 3, tn = lane & 7;
-    const int a_row0 = 32 * wm + tm;
-    const int b_col0 = 64 * wn + 4 * tn;
-    // 64-byte swizzle: 16-byte chunk c of tile row r sits at chunk c ^ ((r >> 1) & 3).
-    // For r = a_row0 + 4i this is (tm >> 1) ^ (2 * (i & 1)).
-    // 128-byte swizzle (kBK = 32): chunk c of tile row r sits at c ^ (r & 7),
-    // which for r = a_row0 + 4i is tm ^ (4 * (i & 1)).
-    const int swz_even = kBK == 16 ? (tm >> 1) : tm;
-
-    // acc[i][p]: row a_row0 + 4i, columns b_col0 + 2p, +1 (p < 2) and
-    // b_col0 + 32 + 2(p-2), +1 (p >= 2).  Pairs of columns are updated by one
-    // paired FMA (fma.rn.f32x2): each lane is an ordinary fused multiply-add
-    // with one rounding, exactly as fmaf.
-    float2 acc[8][4];
+__device__ __forceinline__ void zero(Acc& acc) {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
         for (int p = 0; p < 4; ++p) acc[i][p] = make_float2(0.0f, 0.0f);
+}
 
-    bool ok = true;
-    int s = 0;
-    uint32_t phase = 0;
-    for (int kt = 0; kt < KT; ++kt) {
-        // Refill the stage drained in the previous phase with phase kt-1+kStages.
-        if (tid == 0 && kt > 0) {
-            const int next = kt - 1 + kStages;
-            if (next < KT) {
-                const int ps = (kt - 1) % kStages;
-                const uint32_t pph = static_cast<uint32_t>((kt - 1) / kStages) & 1u;
-                if (!mbar_wait(&empty[ps], pph, status)) { ok = false; break; }
-                mbar_arrive_expect_tx(&full[ps], kStageA + kStageB);
-                tma_load_2d(sA + ps * (kBM * kBK), &tmA, &full[ps], next * kBK, m0);
-                tma_load_2d(sB + ps * (kBK * kBN), &tmB, &full[ps], n0, next * kBK);
-            }
-        }
-        if (!mbar_wait(&full[s], phase, status)) { ok = false; break; }
-
-        const float* As = sA + s * (kBM * kBK);
-        const float* Bs = sB + s * (kBK * kBN);
-        // Per 4 k-values: the thread's rows in groups of kRowGroup, one 128-bit A
-        // read per row (4 consecutive k), two 128-bit B reads per k and group.
+// One k-phase (kBK terms) from a staged A tile (rows of kBK floats, swizzled)
+// and B tile (kBK rows of kBN floats).  Per 4 k-values: the thread's rows in
+// groups of kRowGroup, one 128-bit A read per row (4 consecutive k), two
+// 128-bit B reads per k and group.
+__device__ __forceinline__ void fma_phase(Acc& acc, const float* As, const float* Bs, int a_row0, int b_col0,
+                                          int swz_even) {
 #pragma unroll kChunkUnroll
-        for (int kc = 0; kc < kBK / 4; ++kc) {
+    for (int kc = 0; kc < kBK / 4; ++kc) {
 #pragma unroll
-            for (int g = 0; g < 8 / kRowGroup; ++g) {
-                float4 av[kRowGroup];
+        for (int g = 0; g < 8 / kRowGroup; ++g) {
+            float4 av[kRowGroup];
+#pragma unroll
+            for (int ii = 0; ii < kRowGroup; ++ii) {
+                const int i = kRowGroup * g + ii;
+                const int r = a_row0 + 4 * i;
+                const int chunk = kc ^ (swz_even ^ ((i & 1) << (kBK == 16 ? 1 : 2)));
+                av[ii] = *reinterpret_cast<const float4*>(As + r * kBK + chunk * 4);
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float* brow = Bs + (kc * 4 + kk) * kBN + b_col0;
+                const float4 b0 = *reinterpret_cast<const float4*>(brow);
+                const float4 b1 = *reinterpret_cast<const float4*>(brow + 32);
+                const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
+                                      make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
 #pragma unroll
                 for (int ii = 0; ii < kRowGroup; ++ii) {
-                    const int i = kRowGroup * g + ii;
-                    const int r = a_row0 + 4 * i;
-                    const int chunk = kc ^ (swz_even ^ ((i & 1) << (kBK == 16 ? 1 : 2)));
-                    av[ii] = *reinterpret_cast<const float4*>(As + r * kBK + chunk * 4);
-                }
+                    const float a = kk == 0 ? av[ii].x : kk == 1 ? av[ii].y : kk == 2 ? av[ii].z : av[ii].w;
+                    const float2 aa = make_float2(a, a);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk) {
-                    const float* brow = Bs + (kc * 4 + kk) * kBN + b_col0;
-                    const float4 b0 = *reinterpret_cast<const float4*>(brow);
-                    const float4 b1 = *reinterpret_cast<const float4*>(brow + 32);
-                    const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
-                                          make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
-#pragma unroll
-                    for (int ii = 0; ii < kRowGroup; ++ii) {
-                        const float a = kk == 0 ? av[ii].x : kk == 1 ? av[ii].y : kk == 2 ? av[ii].z : av[ii].w;
-                        const float2 aa = make_float2(a, a);
-#pragma unroll
-                        for (int p = 0; p < 4; ++p)
-                            acc[kRowGroup * g + ii][p] = __ffma2_rn(aa, bp[p], acc[kRowGroup * g + ii][p]);
-                    }
+                    for (int p = 0; p < 4; ++p)
+                        acc[kRowGroup * g + ii][p] = __ffma2_rn(aa, bp[p], acc[kRowGroup * g + ii][p]);
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (++s == kStages) { s = 0; phase ^= 1u; }
     }
-    if (!ok) return;   // status already records the timeout; C is left unwritten
+}
 
-    // Epilogue: every element written exactly once.
+// Writes the thread's part of the tile at (m0, n0); every element of C is
+// written exactly once, rows and columns outside C are skipped.
+__device__ __forceinline__ void store_tile(const Acc& acc, float* C, int64_t ldc, int M, int N, int m0, int n0,
+                                           int a_row0, int b_col0, int vec_store) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int gm = m0 + a_row0 + 4 * i;
@@ -223,8 +172,311 @@ ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     }
 }
 
+// Shared-memory layout of both kernels: kStages A stages, kStages B stages,
+// then the full and empty mbarriers, from a 1024-byte aligned base.
 template <int WR>
-cudaError_t launch_wr(const Problem& p, const Device& dev) {
+struct Smem {
+    float* sA;
+    float* sB;
+    uint64_t* full;
+    uint64_t* empty;
+    __device__ __forceinline__ explicit Smem(uint8_t* raw) {
+        uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+        sA = reinterpret_cast<float*>(base);
+        sB = reinterpret_cast<float*>(base + kStages * FCfg<WR>::STAGE_A);
+        full = reinterpret_cast<uint64_t*>(base + kStages * (FCfg<WR>::STAGE_A + kStageB));
+        empty = full + kStages;
+    }
+};
+
+// Data-parallel form: one CTA per C tile, which walks all of its k-phases.
+template <int WR>
+__global__ void __launch_bounds__(FCfg<WR>::THREADS, FCfg<WR>::MIN_BLOCKS)
+ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                float* __restrict__ C, int64_t ldc, int M, int N, int K, int vec_store, uint32_t* status) {
+    using F = FCfg<WR>;
+    constexpr int kBM = F::BM;
+    extern __shared__ uint8_t smem_raw[];
+    const Smem<WR> sm(smem_raw);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    int tile_m, tile_n;
+    tile_coords(blockIdx.x, (M + kBM - 1) / kBM, (N + kBN - 1) / kBN, tile_m, tile_n);
+    const int m0 = tile_m * kBM;
+    const int n0 = tile_n * kBN;
+    const int KT = (K + kBK - 1) / kBK;
+
+    auto issue = [&](int slot, int kt) {
+        mbar_arrive_expect_tx(&sm.full[slot], F::STAGE_A + kStageB);
+        tma_load_2d(sm.sA + slot * (kBM * kBK), &tmA, &sm.full[slot], kt * kBK, m0);
+        tma_load_2d(sm.sB + slot * (kBK * kBN), &tmB, &sm.full[slot], n0, kt * kBK);
+    };
+    if (tid == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], F::WARPS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int s = 0; s < min(KT, kStages); ++s) issue(s, s);
+
+    // Thread layout: warp (wm, wn) covers rows 32*wm .. +31 and columns
+    // 64*wn .. +63; lane (tm, tn) takes rows tm + 4i (i < 8) and columns
+    // 4*tn .. +3 and 32 + 4*tn .. +3 of that warp tile.
+    const int wm = warp >> 1, wn = warp & 1;
+    const int tm = lane >> 3, tn = lane & 7;
+    const int a_row0 = 32 * wm + tm;
+    const int b_col0 = 64 * wn + 4 * tn;
+    // 64-byte swizzle: 16-byte chunk c of tile row r sits at chunk c ^ ((r >> 1) & 3).
+    // For r = a_row0 + 4i this is (tm >> 1) ^ (2 * (i & 1)).
+    // 128-byte swizzle (kBK = 32): chunk c of tile row r sits at c ^ (r & 7),
+    // which for r = a_row0 + 4i is tm ^ (4 * (i & 1)).
+    const int swz_even = kBK == 16 ? (tm >> 1) : tm;
+
+    Acc acc;
+    zero(acc);
+    bool ok = true;
+    int s = 0;
+    uint32_t phase = 0;
+    for (int kt = 0; kt < KT; ++kt) {
+        // Refill the stage drained in the previous phase with phase kt-1+kStages.
+        if (tid == 0 && kt > 0) {
+            const int next = kt - 1 + kStages;
+            if (next < KT) {
+                const int ps = (kt - 1) % kStages;
+                const uint32_t pph = static_cast<uint32_t>((kt - 1) / kStages) & 1u;
+                if (!mbar_wait(&sm.empty[ps], pph, status)) { ok = false; break; }
+                issue(ps, next);
+            }
+        }
+        if (!mbar_wait(&sm.full[s], phase, status)) { ok = false; break; }
+        fma_phase(acc, sm.sA + s * (kBM * kBK), sm.sB + s * (kBK * kBN), a_row0, b_col0, swz_even);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[s]);
+        if (++s == kStages) { s = 0; phase ^= 1u; }
+    }
+    if (!ok) return;   // status already records the timeout; C is left unwritten
+    store_tile(acc, C, ldc, M, N, m0, n0, a_row0, b_col0, vec_store);
+}
+
+// The work of one CTA of the persistent kernel, as a sequence of segments
+// (tile t, k-phases [ka, kz)).  With G CTAs and T tiles, T = q G + r:
+//  * r = 0, or r k-phase counts too few to share (r KT < G): q (or q + 1 for
+//    CTAs b < r) whole tiles b, b + G, b + 2G, ... -- the CTAs running
+//    together work on G consecutive tiles, which share A and B in L2;
+//  * otherwise q - 1 such rounds, then the last G + r tiles are cut into G
+//    equal runs of (tile, k-phase) iterations ("stream-K"), CTA b taking the
+//    b-th run, so no SM idles in a last partial wave.  Each run is longer
+//    than a tile, so a tile is shared by at most two CTAs: the first segment
+//    of run b + 1 may be a tail (ka > 0) and the last segment of run b a
+//    head (kz < KT) of the same tile.
+struct SkPlan {
+    int n_dp, t_sk0;
+    int64_t v0, v1;   // stream-K run: iterations [v0, v1) of the region starting at tile t_sk0
+
+    __device__ __forceinline__ void init(int tiles, int KT, int b, int G) {
+        int rounds = tiles / G, r = tiles % G, tiles_sk = 0;
+        if (r > 0 && rounds >= 1 && static_cast<int64_t>(r) * KT >= G) {
+            tiles_sk = G + r;
+            rounds -= 1;
+            r = 0;
+        }
+        n_dp = rounds + (b < r ? 1 : 0);
+        t_sk0 = tiles - tiles_sk;
+        const int64_t U = static_cast<int64_t>(tiles_sk) * KT;
+        v0 = U * b / G;
+        v1 = U * (b + 1) / G;
+    }
+    __device__ __forceinline__ int iterations(int KT) const { return n_dp * KT + static_cast<int>(v1 - v0); }
+};
+
+// A position in a CTA's SkPlan sequence: whole tiles done, then the next
+// stream-K iteration.
+struct SkCursor {
+    int j;
+    int64_t v;
+    __device__ __forceinline__ void init(const SkPlan& pl) {
+        j = 0;
+        v = pl.v0;
+    }
+    // Next segment (tile t, k-phases [ka, kz)); false when there is none.
+    __device__ __forceinline__ bool next(const SkPlan& pl, int KT, int& t, int& ka, int& kz) {
+        if (j < pl.n_dp) {
+            t = blockIdx.x + j * gridDim.x;
+            ka = 0;
+            kz = KT;
+            ++j;
+            return true;
+        }
+        if (v >= pl.v1) return false;
+        const int64_t q = v / KT;
+        t = pl.t_sk0 + static_cast<int>(q);
+        ka = static_cast<int>(v - q * KT);
+        kz = static_cast<int>(min(static_cast<int64_t>(KT), ka + (pl.v1 - v)));
+        v += kz - ka;
+        return true;
+    }
+};
+
+// Persistent form: one CTA per SM walking its SkPlan sequence; the copy
+// pipeline runs on from one segment into the next.  A tile shared by two
+// CTAs is finished by the one holding its first phases (the head): the other
+// (the tail) writes its partial sums to `ws` and raises its flag, and the C
+// value is (head partial) + (tail partial), always in that order.  The launch
+// is cooperative, so every CTA is resident and a head's wait for its tail
+// ends.
+__global__ void __launch_bounds__(FCfg<4>::THREADS, 1)
+ffma_f32_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   float* __restrict__ C, int64_t ldc, int M, int N, int K, int vec_store, uint32_t* status,
+                   float* __restrict__ ws, unsigned* __restrict__ flags) {
+    using F = FCfg<4>;
+    constexpr int kBM = F::BM;
+    extern __shared__ uint8_t smem_raw[];
+    const Smem<4> sm(smem_raw);
+    __shared__ int s_flag_ok;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int tiles_m = (M + kBM - 1) / kBM;
+    const int tiles_n = (N + kBN - 1) / kBN;
+    const int KT = (K + kBK - 1) / kBK;
+    // The plan and the producer's cursor are read once per segment, so they
+    // live in shared memory rather than in registers through the k loop.
+    __shared__ SkPlan s_plan;
+    __shared__ SkCursor s_pc;
+    int NI;
+    {
+        SkPlan plan;
+        plan.init(tiles_m * tiles_n, KT, blockIdx.x, gridDim.x);
+        NI = plan.iterations(KT);
+        if (tid == 0) {
+            s_plan = plan;
+            s_pc.init(plan);
+        }
+    }
+
+    // Producer (thread 0): its own cursor, up to kStages iterations ahead of
+    // the consumers'; the tile origin is recomputed once per segment.
+    int p_kb = 0, p_kz = 0, p_m0 = 0, p_n0 = 0;
+    auto issue_next = [&](int slot) {
+        if (p_kb == p_kz) {
+            int t;
+            s_pc.next(s_plan, KT, t, p_kb, p_kz);
+            int tm_, tn_;
+            tile_coords(t, tiles_m, tiles_n, tm_, tn_);
+            p_m0 = tm_ * kBM;
+            p_n0 = tn_ * kBN;
+        }
+        mbar_arrive_expect_tx(&sm.full[slot], F::STAGE_A + kStageB);
+        tma_load_2d(sm.sA + slot * (kBM * kBK), &tmA, &sm.full[slot], p_kb * kBK, p_m0);
+        tma_load_2d(sm.sB + slot * (kBK * kBN), &tmB, &sm.full[slot], p_n0, p_kb * kBK);
+        ++p_kb;
+    };
+    if (tid == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], F::WARPS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int s = 0; s < min(NI, kStages); ++s) issue_next(s);
+
+    // Thread layout and swizzle as in the data-parallel kernel.
+    const int wm = warp >> 1, wn = warp & 1;
+    const int tm = lane >> 3, tn = lane & 7;
+    const int a_row0 = 32 * wm + tm;
+    const int b_col0 = 64 * wn + 4 * tn;
+    const int swz_even = kBK == 16 ? (tm >> 1) : tm;
+
+    bool ok = true;
+    int s = 0;
+    uint32_t phase = 0;
+    int it = 0;                                   // iterations consumed so far
+    SkCursor cc;
+    cc.init(s_plan);
+    int t, ka, kz;
+    while (cc.next(s_plan, KT, t, ka, kz)) {
+        const int seg_end = it + (kz - ka);
+        Acc acc;
+        zero(acc);
+        for (; it < seg_end; ++it) {
+            // Refill the stage drained in the previous iteration with iteration
+            // it-1+kStages.  A thread whose wait ran out stops waiting (and
+            // issuing) but keeps the others' control flow, so every
+            // __syncthreads below is reached.
+            if (tid == 0 && it > 0) {
+                const int next = it - 1 + kStages;
+                if (next < NI && ok) {
+                    const int ps = (it - 1) % kStages;
+                    const uint32_t pph = static_cast<uint32_t>((it - 1) / kStages) & 1u;
+                    if (mbar_wait(&sm.empty[ps], pph, status)) issue_next(ps);
+                    else ok = false;
+                }
+            }
+            if (!mbar_try_wait(smem_addr(&sm.full[s]), phase) && ok) ok = mbar_wait(&sm.full[s], phase, status);
+            fma_phase(acc, sm.sA + s * (kBM * kBK), sm.sB + s * (kBK * kBN), a_row0, b_col0, swz_even);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            if (++s == kStages) { s = 0; phase ^= 1u; }
+        }
+
+        int tile_m, tile_n;
+        tile_coords(t, tiles_m, tiles_n, tile_m, tile_n);
+        if (ka > 0) {
+            // Tail: hand the 64 partial sums of each thread to the previous CTA.
+            // float4 j of thread tid goes to j * THREADS + tid, so a warp stores
+            // 512 contiguous bytes.
+            float4* dst = reinterpret_cast<float4*>(ws + static_cast<int64_t>(blockIdx.x) * kBM * kBN) + tid;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int p = 0; p < 4; p += 2)
+                    dst[(i * 2 + p / 2) * F::THREADS] =
+                        make_float4(acc[i][p].x, acc[i][p].y, acc[i][p + 1].x, acc[i][p + 1].y);
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) st_release_u32(flags + blockIdx.x, 1u);
+            continue;
+        }
+        if (kz < KT) {
+            // Head: wait for the next CTA's tail of this tile and add it.
+            if (tid == 0) s_flag_ok = ok && wait_flag(flags + blockIdx.x + 1, status) ? 1 : 0;
+            __syncthreads();
+            if (s_flag_ok) {
+                const float4* src =
+                    reinterpret_cast<const float4*>(ws + static_cast<int64_t>(blockIdx.x + 1) * kBM * kBN) + tid;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int p = 0; p < 4; p += 2) {
+                        const float4 v = __ldcg(src + (i * 2 + p / 2) * F::THREADS);
+                        acc[i][p].x += v.x;
+                        acc[i][p].y += v.y;
+                        acc[i][p + 1].x += v.z;
+                        acc[i][p + 1].y += v.w;
+                    }
+            }
+        }
+        store_tile(acc, C, ldc, M, N, tile_m * kBM, tile_n * kBN, a_row0, b_col0, vec_store);
+    }
+    (void)ok;   // on a timeout the status word records it and C is incomplete
+}
+
+// Launches the data-parallel kernel (workspace == nullptr) or, with its
+// workspace, the stream-K kernel (WR = 4).
+template <int WR>
+cudaError_t launch_wr(const Problem& p, const Device& dev, void* workspace) {
     using F = FCfg<WR>;
     CUtensorMap ta, tb;
     if (!make_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.A, p.m, p.k, p.lda, F::BM, kBK,
@@ -232,20 +484,46 @@ cudaError_t launch_wr(const Problem& p, const Device& dev) {
         !make_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.k, p.n, p.ldb, kBK, kBN,
                          CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    auto kernel = ffma_f32_kernel<WR>;
+    const bool sk = workspace != nullptr;
+    const void* kernel = sk ? reinterpret_cast<const void*>(ffma_f32_sk_kernel)
+                            : reinterpret_cast<const void*>(ffma_f32_kernel<WR>);
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(F::SMEM));
     if (err != cudaSuccess) {
-        set_error("cudaFuncSetAttribute(ffma_f32_kernel): %s", cudaGetErrorString(err));
+        set_error("cudaFuncSetAttribute(ffma_f32 kernel): %s", cudaGetErrorString(err));
         return err;
     }
     const int64_t tiles = static_cast<int64_t>((p.m + F::BM - 1) / F::BM) * ((p.n + kBN - 1) / kBN);
     const int vec_store = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
-    kernel<<<static_cast<unsigned>(tiles), F::THREADS, F::SMEM, p.stream>>>(ta, tb, p.C, p.ldc, p.m, p.n, p.k,
-                                                                            vec_store, dev.status);
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(F::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = F::SMEM;
+    cfg.stream = p.stream;
+    if (!sk) {
+        cfg.gridDim = dim3(static_cast<unsigned>(tiles), 1, 1);
+        err = cudaLaunchKernelEx(&cfg, ffma_f32_kernel<WR>, ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store,
+                                 dev.status);
+    } else {
+        // one partial tile and one flag per CTA; the flags start cleared
+        const unsigned grid = static_cast<unsigned>(dev.sm_count);
+        float* ws = static_cast<float*>(workspace);
+        unsigned* flags = reinterpret_cast<unsigned*>(ws + static_cast<size_t>(grid) * F::BM * kBN);
+        err = cudaMemsetAsync(flags, 0, grid * sizeof(unsigned), p.stream);
+        if (err != cudaSuccess) {
+            set_error("stream-K flags: %s", cudaGetErrorString(err));
+            return err;
+        }
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: a head may wait for its tail
+        attr[0].val.cooperative = 1;
+        cfg.gridDim = dim3(grid, 1, 1);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        err = cudaLaunchKernelEx(&cfg, ffma_f32_sk_kernel, ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store,
+                                 dev.status, ws, flags);
+    }
     count_launch();
-    err = cudaGetLastError();
-    if (err != cudaSuccess) set_error("ffma_f32_kernel launch: %s", cudaGetErrorString(err));
+    if (err != cudaSuccess) set_error("ffma_f32 kernel launch: %s", cudaGetErrorString(err));
     return err;
 }
 
@@ -253,10 +531,40 @@ cudaError_t launch_wr(const Problem& p, const Device& dev) {
 // 64-row CTAs per SM; 4097 x 3001 x 1024 42.8 vs 46.3.
 constexpr int kShortK = 2048;
 
+// The persistent kernel when k is long, the one-tile-per-CTA grid would
+// leave at least a tenth of its CTA slots empty (tiles / (waves * G) < 0.9),
+// and the plan has a stream-K region (same rule as SkPlan).  Measured on
+// GB300 (TFLOP/s, one-tile grid -> persistent): 2500 x 2000 x 2300 (2.1
+// waves) 37.6 -> 48.7; 2000 x 2000 x 4096 (1.7 waves) 43.6 -> 46.7; but
+// 4096^3 (6.7 waves) 53.1 -> 50.7 and 3000 x 6000 x 4096 (7.4 waves)
+// 50.5 -> 49.4, where the one-tile grid's loop runs faster.
+bool use_stream_k(const Problem& p, const Device& dev) {
+    if (p.k < kShortK) return false;
+    const int64_t G = dev.sm_count;
+    const int64_t tiles = static_cast<int64_t>((p.m + 127) / 128) * ((p.n + kBN - 1) / kBN);
+    const int64_t KT = (p.k + kBK - 1) / kBK;
+    const int64_t rounds = tiles / G, r = tiles % G;
+    const int64_t waves = (tiles + G - 1) / G;
+    return rounds >= 1 && r > 0 && r * KT >= G && 10 * tiles < 9 * waves * G;
+}
+
 }  // namespace
 
-cudaError_t launch_ffma_f32(const Problem& p, const Device& dev) {
-    return p.k < kShortK ? launch_wr<2>(p, dev) : launch_wr<4>(p, dev);
+uint64_t ffma_f32_workspace_bytes(const Problem& p, const Device& dev) {
+    if (!use_stream_k(p, dev)) return 0;
+    return static_cast<uint64_t>(dev.sm_count) * (FCfg<4>::BM * kBN * sizeof(float) + sizeof(unsigned));
+}
+
+cudaError_t launch_ffma_f32(const Problem& p, const Device& dev, void* workspace) {
+    if (p.k < kShortK) return launch_wr<2>(p, dev, nullptr);
+    if (use_stream_k(p, dev)) {
+        if (!workspace) {
+            set_error("ffma_f32: stream-K form launched without its workspace");
+            return cudaErrorInvalidValue;
+        }
+        return launch_wr<4>(p, dev, workspace);
+    }
+    return launch_wr<4>(p, dev, nullptr);
 }
 
 }  // namespace tgemm

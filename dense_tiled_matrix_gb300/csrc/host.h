@@ -64,7 +64,11 @@ bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb);
 // Each returns cudaSuccess or the launch error (with set_error called).
 
 // fp32 FFMA kernel; A and B must be 16-byte aligned with 16-byte row pitches.
-cudaError_t launch_ffma_f32(const Problem& p, const Device& dev);
+// Shapes that take its split-tile form need ffma_f32_workspace_bytes() of
+// stream-ordered device memory (256-byte aligned, no initial contents), valid
+// until the kernel has run; others need none and take nullptr.
+uint64_t ffma_f32_workspace_bytes(const Problem& p, const Device& dev);
+cudaError_t launch_ffma_f32(const Problem& p, const Device& dev, void* workspace);
 
 // tcgen05 kernels; same alignment rule.  `tf32` selects kind::tf32 on fp32
 // inputs, and then p.B must hold B TRANSPOSED (n x k, pitch p.ldb, k

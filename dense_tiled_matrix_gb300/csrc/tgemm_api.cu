@@ -247,14 +247,17 @@ tgemm_status run(Kind kind, int64_t m, int64_t n, int64_t k, const void* A, int6
         b_ld2 = (n + align_elems - 1) / align_elems * align_elems;
         b_ws = static_cast<uint64_t>(k) * b_ld2 * es;
     }
+    // The fp32 kernel's split tiles need room for partial sums (size known from the shape).
+    const uint64_t c_ws = kind == Kind::F32 ? ffma_f32_workspace_bytes(p, *dev) : 0;
     void* work = nullptr;
     cudaError_t err = cudaSuccess;
-    if (a_ws + b_ws > 0) {
-        const uint64_t b_off = (a_ws + 255) / 256 * 256;
-        err = cudaMallocAsync(&work, b_off + b_ws, stream);
+    const uint64_t b_off = (a_ws + 255) / 256 * 256;
+    const uint64_t c_off = (b_off + b_ws + 255) / 256 * 256;
+    if (a_ws + b_ws + c_ws > 0) {
+        err = cudaMallocAsync(&work, c_off + c_ws, stream);
         if (err != cudaSuccess) {
             cudaGetLastError();
-            set_error("workspace of %llu bytes: %s", (unsigned long long)(b_off + b_ws), cudaGetErrorString(err));
+            set_error("workspace of %llu bytes: %s", (unsigned long long)(c_off + c_ws), cudaGetErrorString(err));
             return TGEMM_ERR_WORKSPACE;
         }
         uint8_t* w = static_cast<uint8_t*>(work);
@@ -279,7 +282,7 @@ tgemm_status run(Kind kind, int64_t m, int64_t n, int64_t k, const void* A, int6
             set_error("problem too large: %lld output tiles", (long long)(tiles_m * tiles_n));
             st = TGEMM_ERR_INVALID_VALUE;
         } else if (kind == Kind::F32) {
-            err = launch_ffma_f32(p, *dev);
+            err = launch_ffma_f32(p, *dev, c_ws ? static_cast<uint8_t*>(work) + c_off : nullptr);
         } else if (kind == Kind::BF16 && m <= 64) {
             err = launch_umma_skinny(p, *dev);
         } else {

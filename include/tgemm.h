@@ -21,7 +21,9 @@
  * never frees them and keeps no reference after the call returns.  The
  * library may take temporary stream-ordered workspace on `stream` (for
  * operands whose base address or leading dimension is not a multiple of 16
- * bytes) and returns it on the same stream.
+ * bytes, for B transposed on the TF32 path, and for the partial sums of
+ * tiles that tgemm_f32 splits between two blocks) and returns it on the same
+ * stream.
  *
  * Execution.  Every call is asynchronous on `stream` (NULL is the legacy
  * default stream) and returns once the work is queued.  Argument errors are

@@ -69,6 +69,25 @@ def test_irregular_4097x3001x1023(mode):
     parity.full_check(mode, inputs.make("irregular"))
 
 
+# The fp32 kernel's persistent form (k >= 2048, and a one-tile-per-CTA grid
+# would leave at least a tenth of its slots empty): rounds of whole tiles,
+# then a stream-K region where tiles are split between two CTAs and the CTA
+# holding a tile's first k-phases adds the other's partial sums.  One round,
+# one round, no round, three rounds before the stream-K region; ragged in m,
+# n and k, checked over the whole output.
+STREAM_K_SHAPES = [(2432, 2100, 2050), (2500, 2000, 2300), (2000, 2000, 4100), (500, 20000, 2050)]
+
+
+@pytest.mark.parametrize("shape", STREAM_K_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_fp32_persistent_schedule(shape):
+    m, n, k = shape
+    parity.full_check("f32", inputs.random_case(7000 + m + n + k, m, n, k, kind="int"), f"f32 int {shape}")
+    case = inputs.random_case(8000 + m + n + k, m, n, k, kind="uniform")
+    parity.full_check("f32", case, f"f32 uniform {shape}")
+    A, B = parity.to_device(case.A), parity.to_device(case.B)
+    assert torch.equal(parity.ENTRY["f32"](A, B), parity.ENTRY["f32"](A, B))
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_leading_dimensions_and_untouched_padding(mode):
     m, n, k = 200, 150, 90
