@@ -10,11 +10,8 @@
 // instead of replaying 32 times on one bank; blocks of 32 x 8 threads each move
 // 4 elements per tile to amortise index arithmetic.
 //
-// When both matrices are 16-byte aligned with 16-byte pitches, a wider form
-// moves the data with 128-bit accesses: a 64 x 32 tile per 256 threads, each
-// thread loading two float4 from input rows and storing two float4 to output
-// rows; the tile is [64][33], so both the row-wise writes into it and the
-// column-wise reads out of it hit 32 distinct banks per warp instruction.
+// When both matrices are 16-byte aligned with 16-byte pitches, a TMA form
+// (below) moves whole 128-byte lines in and out instead.
 #include "device.cuh"
 #include "host.h"
 
@@ -49,72 +46,113 @@ transpose_kernel(const uint32_t* __restrict__ src, int64_t ld_src, uint32_t* __r
     }
 }
 
-constexpr int kVRows = 64;   // input rows per tile of the 128-bit form
-constexpr int kVCols = 32;   // input columns per tile
+// TMA form: a persistent grid whose CTAs take 128 x 32 input tiles (128 rows
+// of one 128-byte line each) in turn.  One thread keeps kXStages tile loads in
+// flight (TMA with the 128-byte swizzle: 16-byte chunk c of tile row r sits at
+// chunk c ^ (r % 8), so the 8 lanes of a quarter-warp reading chunk j of 8
+// consecutive rows hit 8 different bank groups); the CTA turns each tile into
+// a 32 x 128 output tile in a plain shared buffer (a warp writes 32
+// consecutive words per instruction) and one thread stores it with a TMA bulk
+// store, which skips rows and columns outside dst.  Two output buffers
+// alternate, so a tile's store overlaps the next tile's shuffle.
+constexpr int kXR = 128;                               // input rows per tile = output columns
+constexpr int kXC = 32;                                // input columns per tile = output rows
+constexpr int kXStages = 4;
+constexpr int kXThreads = 256;
+constexpr uint32_t kXTileBytes = kXR * kXC * 4;        // 16 KiB
+constexpr size_t kXSmem = 1024 + (kXStages + 2) * kXTileBytes + kXStages * sizeof(uint64_t);
 
-__global__ void __launch_bounds__(256)
-transpose_v4_kernel(const float* __restrict__ src, int64_t ld_src, float* __restrict__ dst, int64_t ld_dst,
-                    int rows, int cols) {
-    __shared__ float tile[kVRows][kVCols + 1];
-    const int t = threadIdx.x;
-    const int lr = t >> 3;         // input row (and output row) within a 32-row half / the tile
-    const int lq = (t & 7) * 4;    // first of 4 consecutive elements
-    const int64_t tiles_c = (cols + kVCols - 1) / kVCols;
-    const int64_t tiles = tiles_c * ((rows + kVRows - 1) / kVRows);
-    for (int64_t idx = blockIdx.x; idx < tiles; idx += gridDim.x) {
-        const int r0 = static_cast<int>(idx / tiles_c) * kVRows;
-        const int c0 = static_cast<int>(idx % tiles_c) * kVCols;
-        const bool whole = r0 + kVRows <= rows && c0 + kVCols <= cols;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int r = r0 + lr + 32 * i;
-            if (whole) {
-                const float4 v = __ldg(reinterpret_cast<const float4*>(src + static_cast<int64_t>(r) * ld_src + c0 + lq));
-                tile[lr + 32 * i][lq + 0] = v.x;
-                tile[lr + 32 * i][lq + 1] = v.y;
-                tile[lr + 32 * i][lq + 2] = v.z;
-                tile[lr + 32 * i][lq + 3] = v.w;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int c = c0 + lq + j;
-                    tile[lr + 32 * i][lq + j] = (r < rows && c < cols) ? src[static_cast<int64_t>(r) * ld_src + c] : 0.0f;
-                }
-            }
-        }
-        __syncthreads();
-        const int c = c0 + lr;   // output row
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int rr = lq + 32 * i;   // first of 4 output columns (input rows) within the tile
-            if (whole) {
-                const float4 w = make_float4(tile[rr][lr], tile[rr + 1][lr], tile[rr + 2][lr], tile[rr + 3][lr]);
-                *reinterpret_cast<float4*>(dst + static_cast<int64_t>(c) * ld_dst + r0 + rr) = w;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int r = r0 + rr + j;
-                    if (c < cols && r < rows) dst[static_cast<int64_t>(c) * ld_dst + r] = tile[rr + j][lr];
-                }
-            }
-        }
-        __syncthreads();
+__global__ void __launch_bounds__(kXThreads, 2)
+transpose_tma_kernel(const __grid_constant__ CUtensorMap tm_src, const __grid_constant__ CUtensorMap tm_dst,
+                     int rows, int cols, uint32_t* status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* in = base;                                           // kXStages swizzled input tiles
+    float* out = reinterpret_cast<float*>(base + kXStages * kXTileBytes);   // 2 x [kXC][kXR]
+    uint64_t* full = reinterpret_cast<uint64_t*>(base + (kXStages + 2) * kXTileBytes);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tiles_c = (cols + kXC - 1) / kXC;
+    const int64_t tiles = static_cast<int64_t>((rows + kXR - 1) / kXR) * tiles_c;
+    const int n = tiles > blockIdx.x ? static_cast<int>((tiles - 1 - blockIdx.x) / gridDim.x) + 1 : 0;
+    auto load = [&](int i) {
+        const int64_t t = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+        const int s = i % kXStages;
+        mbar_arrive_expect_tx(&full[s], kXTileBytes);
+        tma_load_2d(in + s * kXTileBytes, &tm_src, &full[s], static_cast<int>(t % tiles_c) * kXC,
+                    static_cast<int>(t / tiles_c) * kXR);
+    };
+    if (tid == 0) {
+        tma_prefetch_map(&tm_src);
+        tma_prefetch_map(&tm_dst);
+        for (int s = 0; s < kXStages; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+        for (int i = 0; i < n && i < kXStages; ++i) load(i);
     }
+    __syncthreads();
+
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+        const int s = i % kXStages;
+        float* o = out + (i & 1) * (kXC * kXR);
+        if (ok && !mbar_wait(&full[s], static_cast<uint32_t>(i / kXStages) & 1u, status)) ok = false;
+        if (tid == 0) bulk_wait_group_read<1>();   // the store that last used `o` has read it
+        __syncthreads();
+        // Warp w moves 4 strips of 32 rows x 4 columns: lane l reads row
+        // 32 rb + l, chunk j (columns 4j .. 4j+3) and writes them to output
+        // rows 4j .. 4j+3, column 32 rb + l.
+        const uint8_t* tile = in + s * kXTileBytes;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int u = warp * 4 + q, rb = u >> 3, j = u & 7;
+            const int r = rb * 32 + lane;
+            const float4 v = *reinterpret_cast<const float4*>(tile + r * 128 + ((j ^ (r & 7)) << 4));
+            o[(4 * j + 0) * kXR + r] = v.x;
+            o[(4 * j + 1) * kXR + r] = v.y;
+            o[(4 * j + 2) * kXR + r] = v.z;
+            o[(4 * j + 3) * kXR + r] = v.w;
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            const int64_t t = blockIdx.x + static_cast<int64_t>(i) * gridDim.x;
+            tma_store_2d(&tm_dst, o, static_cast<int>(t / tiles_c) * kXR, static_cast<int>(t % tiles_c) * kXC);
+            bulk_commit_group();
+            // Every thread has read stage s (barrier above): refill it.
+            if (ok && i + kXStages < n) {
+                fence_proxy_async_smem();
+                load(i + kXStages);
+            }
+        }
+    }
+    if (tid == 0) bulk_wait_group<0>();
 }
 
 }  // namespace
 
 cudaError_t launch_transpose(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows,
                              int64_t cols, cudaStream_t stream, const Device& dev) {
-    const bool v4 = reinterpret_cast<uintptr_t>(src) % 16 == 0 && reinterpret_cast<uintptr_t>(dst) % 16 == 0 &&
-                    ld_src % 4 == 0 && ld_dst % 4 == 0;
-    if (v4) {
-        const int64_t tiles = ((rows + kVRows - 1) / kVRows) * ((cols + kVCols - 1) / kVCols);
-        const int64_t cap = static_cast<int64_t>(dev.sm_count) * 8;
+    const bool aligned = reinterpret_cast<uintptr_t>(src) % 16 == 0 && reinterpret_cast<uintptr_t>(dst) % 16 == 0 &&
+                         ld_src % 4 == 0 && ld_dst % 4 == 0;
+    cudaError_t err = cudaSuccess;
+    if (aligned) {
+        CUtensorMap ts, td;
+        if (!make_tensor_map(&ts, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, src, rows, cols, ld_src, kXR, kXC,
+                             CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_tensor_map(&td, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dst, cols, rows, ld_dst, kXC, kXR,
+                             CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+        err = cudaFuncSetAttribute(transpose_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(kXSmem));
+        if (err != cudaSuccess) {
+            set_error("cudaFuncSetAttribute(transpose_tma_kernel): %s", cudaGetErrorString(err));
+            return err;
+        }
+        const int64_t tiles = ((rows + kXR - 1) / kXR) * ((cols + kXC - 1) / kXC);
+        const int64_t cap = static_cast<int64_t>(dev.sm_count) * 2;
         const unsigned grid = static_cast<unsigned>(tiles < cap ? tiles : cap);
-        transpose_v4_kernel<<<grid, 256, 0, stream>>>(static_cast<const float*>(src), ld_src,
-                                                       static_cast<float*>(dst), ld_dst, static_cast<int>(rows),
-                                                       static_cast<int>(cols));
+        transpose_tma_kernel<<<grid, kXThreads, kXSmem, stream>>>(ts, td, static_cast<int>(rows),
+                                                                  static_cast<int>(cols), dev.status);
     } else {
         const int64_t tiles = ((rows + kTile - 1) / kTile) * ((cols + kTile - 1) / kTile);
         const int64_t cap = static_cast<int64_t>(dev.sm_count) * 64;
@@ -124,7 +162,7 @@ cudaError_t launch_transpose(const void* src, int64_t ld_src, void* dst, int64_t
             static_cast<int>(rows), static_cast<int>(cols));
     }
     count_launch();
-    cudaError_t err = cudaGetLastError();
+    err = cudaGetLastError();
     if (err != cudaSuccess) set_error("transpose kernel launch: %s", cudaGetErrorString(err));
     return err;
 }

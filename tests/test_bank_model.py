@@ -12,7 +12,8 @@ distinct words any bank must deliver.
 
 The FFMA kernel's addressing is restated here from its source and checked to
 need one pass per instruction; the TMA 64-byte swizzle it relies on is
-checked against the kernel's own chunk formula.
+checked against the kernel's own chunk formula.  So are the TMA transpose's
+reads of a 128-byte-swizzled input tile and its writes of the output tile.
 """
 import pytest
 
@@ -133,3 +134,63 @@ def test_ffma_thread_tiles_cover_the_cta_tile_once(warp_rows):
                         assert cell not in seen
                         seen.add(cell)
     assert seen == {(r, c) for r in range(32 * warp_rows) for c in range(128)}
+
+
+# ---- TMA transpose (csrc/transpose.cu): 128 x 32 fp32 input tile, 128-byte swizzle ----
+def swizzle128(offset):
+    """TMA 128-byte swizzle: bits [4,6] of the byte offset XOR bits [7,9]."""
+    return offset ^ (((offset >> 7) & 7) << 4)
+
+
+def transpose_read(warp, lane, q):
+    u = warp * 4 + q
+    rb, j = u >> 3, u & 7
+    r = rb * 32 + lane
+    return r * 128 + ((j ^ (r & 7)) << 4), (r, j)
+
+
+def test_transpose_read_address_is_the_tma_swizzle():
+    for warp in range(8):
+        for lane in range(32):
+            for q in range(4):
+                addr, (r, j) = transpose_read(warp, lane, q)
+                assert addr == swizzle128(r * 128 + j * 16)
+
+
+@pytest.mark.parametrize("warp", range(8))
+def test_transpose_reads_one_pass_per_quarter_warp(warp):
+    # A 128-bit access is served a quarter-warp at a time: each quarter must
+    # touch 8 distinct 16-byte bank groups.
+    for q in range(4):
+        for quarter in range(4):
+            addrs = [transpose_read(warp, lane, q)[0] for lane in range(8 * quarter, 8 * quarter + 8)]
+            assert wavefronts(addrs, width=16) == 1, (warp, q, quarter)
+
+
+def test_transpose_reads_would_conflict_without_the_swizzle():
+    addrs = [(rb * 32 + lane) * 128 + 3 * 16 for rb in [0] for lane in range(8)]
+    assert wavefronts(addrs, width=16) == 8
+
+
+@pytest.mark.parametrize("warp", range(8))
+def test_transpose_writes_one_pass(warp):
+    # Output tile [32][128] floats, unswizzled: lane l writes column 32 rb + l
+    # of output row 4 j + e.
+    for q in range(4):
+        u = warp * 4 + q
+        rb, j = u >> 3, u & 7
+        for e in range(4):
+            addrs = [((4 * j + e) * 128 + rb * 32 + lane) * 4 for lane in range(32)]
+            assert wavefronts(addrs) == 1
+
+
+def test_transpose_strips_cover_the_tile_once():
+    seen = set()
+    for warp in range(8):
+        for lane in range(32):
+            for q in range(4):
+                _, (r, j) = transpose_read(warp, lane, q)
+                for e in range(4):
+                    assert (r, 4 * j + e) not in seen
+                    seen.add((r, 4 * j + e))
+    assert seen == {(r, c) for r in range(128) for c in range(32)}

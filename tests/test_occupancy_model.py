@@ -66,7 +66,7 @@ GB300 = dict(max_threads=2048, max_blocks=32, smem_per_sm=228 * 1024, regs_per_s
     ("ffma_f32_kernel<2>", 128, 50240, 256, 2),
     ("umma_kernel (wide or narrow)", 192, 197728, 56, 1),
     ("umma_skinny_kernel<16>", 128, 74840, 40, 3),
-    ("transpose_v4_kernel", 256, 8448, 32, 8),
+    ("transpose_tma_kernel", 256, 99360, 48, 2),    # 42 registers allocate as 48
 ])
 def test_libtgemm_kernels(name, threads, smem, regs, expect):
     assert blocks_per_sm(threads, smem, regs, **GB300) == expect, name
