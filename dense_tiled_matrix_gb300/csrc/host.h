@@ -63,6 +63,14 @@ bool overlaps(const void* a, uint64_t na, const void* b, uint64_t nb);
 // ------------------------------------------------------------ launchers --
 // Each returns cudaSuccess or the launch error (with set_error called).
 
+// The persistent kernels' plan (stream_k.cuh) has a stream-K region -- T = qG
+// + r tiles on G CTAs with q >= 1, r > 0 and r * KT >= G -- so its last G + r
+// tiles are split along k into G equal runs.
+inline bool sk_has_region(int64_t tiles, int64_t KT, int64_t G) {
+    const int64_t r = tiles % G;
+    return tiles >= G && r > 0 && r * KT >= G;
+}
+
 // fp32 FFMA kernel; A and B must be 16-byte aligned with 16-byte row pitches.
 // Shapes that take its split-tile form need ffma_f32_workspace_bytes() of
 // stream-ordered device memory (256-byte aligned, no initial contents), valid
@@ -72,8 +80,12 @@ cudaError_t launch_ffma_f32(const Problem& p, const Device& dev, void* workspace
 
 // tcgen05 kernels; same alignment rule.  `tf32` selects kind::tf32 on fp32
 // inputs, and then p.B must hold B TRANSPOSED (n x k, pitch p.ldb, k
-// contiguous); otherwise bf16 inputs under kind::f16 with B as k x n.
-cudaError_t launch_umma(const Problem& p, const Device& dev, bool tf32);
+// contiguous); otherwise bf16 inputs under kind::f16 with B as k x n.  With
+// umma_workspace_bytes() of stream-ordered workspace (no initial contents)
+// the last partial wave of tiles is split along k (stream-K); with nullptr
+// whole tiles only.
+uint64_t umma_workspace_bytes(const Problem& p, const Device& dev, bool tf32);
+cudaError_t launch_umma(const Problem& p, const Device& dev, bool tf32, void* workspace);
 
 // bf16 tcgen05 kernel for m <= 64: C^T = B^T A^T with k split across the CTAs
 // of a cluster and the partials added through distributed shared memory.

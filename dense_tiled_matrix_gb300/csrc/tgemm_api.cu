@@ -247,8 +247,12 @@ tgemm_status run(Kind kind, int64_t m, int64_t n, int64_t k, const void* A, int6
         b_ld2 = (n + align_elems - 1) / align_elems * align_elems;
         b_ws = static_cast<uint64_t>(k) * b_ld2 * es;
     }
-    // The fp32 kernel's split tiles need room for partial sums (size known from the shape).
-    const uint64_t c_ws = kind == Kind::F32 ? ffma_f32_workspace_bytes(p, *dev) : 0;
+    // Split tiles of the persistent kernels need room for partial sums (size
+    // known from the shape).
+    const bool skinny = kind == Kind::BF16 && m <= 64;
+    const uint64_t c_ws = kind == Kind::F32 ? ffma_f32_workspace_bytes(p, *dev)
+                          : skinny          ? 0
+                                            : umma_workspace_bytes(p, *dev, kind == Kind::TF32);
     void* work = nullptr;
     cudaError_t err = cudaSuccess;
     const uint64_t b_off = (a_ws + 255) / 256 * 256;
@@ -283,10 +287,10 @@ tgemm_status run(Kind kind, int64_t m, int64_t n, int64_t k, const void* A, int6
             st = TGEMM_ERR_INVALID_VALUE;
         } else if (kind == Kind::F32) {
             err = launch_ffma_f32(p, *dev, c_ws ? static_cast<uint8_t*>(work) + c_off : nullptr);
-        } else if (kind == Kind::BF16 && m <= 64) {
+        } else if (skinny) {
             err = launch_umma_skinny(p, *dev);
         } else {
-            err = launch_umma(p, *dev, kind == Kind::TF32);
+            err = launch_umma(p, *dev, kind == Kind::TF32, c_ws ? static_cast<uint8_t*>(work) + c_off : nullptr);
         }
     }
     if (work) {

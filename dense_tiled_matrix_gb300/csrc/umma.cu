@@ -6,11 +6,13 @@
 // page's Pvalue) moved into tensor memory and the per-phase inner product done
 // by tcgen05.mma:
 //
-//  * Output tiles of 256 x 256 (k >= 3072: two 128-row MMAs share each B tile,
-//    one accumulator spanning all 512 tensor-memory columns, 3 stages) or
-//    128 x 256 (two accumulators, 4 stages), visited by a persistent grid of
-//    one CTA per SM in groups of tile rows (neighbouring CTAs share A and B
-//    tiles in L2).
+//  * Output tiles of 256 x BN (k >= 3072: two 128-row MMAs share each B tile,
+//    one accumulator spanning the tensor memory, 3 stages) or 128 x BN (two
+//    accumulators, 4 stages), BN = 256, or 224 for TF32 shapes whose last wave
+//    that fills better; visited by a persistent grid of one CTA per SM in
+//    groups of tile rows (neighbouring CTAs share A and B tiles in L2).  Where
+//    whole tiles would leave more than a quarter of the CTA slots idle, the
+//    last G + r tiles are split along k between CTAs (stream-K, stream_k.cuh).
 //  * Phases of 128 bytes of K (64 bf16 or 32 fp32 elements).  Warp 0 streams
 //    the A tile (128 x BK, K-major) and the B tile into a 4-stage shared-memory
 //    ring with TMA, 128-byte swizzled so the tensor core reads them without
@@ -30,23 +32,25 @@
 //    128-bit stores, masked at the edges of C.
 //
 // Every C element is written exactly once.  The tensor cores add the k terms
-// in a fixed order, so repeated runs are bit-identical.
+// in a fixed order, and a split tile is (head partial) + (tail partial), so
+// repeated runs are bit-identical.
 #include <cstdio>
 
 #include "device.cuh"
 #include "host.h"
+#include "stream_k.cuh"
 
 namespace tgemm {
 namespace {
 
-template <bool kTF32, bool kBKMajor, bool kWide>
+template <bool kTF32, bool kBKMajor, bool kWide, int kBN = 256>
 struct Cfg {
     // kWide: 256 x 256 C tiles, two 128-row MMAs sharing each B tile, the whole
     // tensor memory as one accumulator; otherwise 128 x 256 tiles with two
     // accumulators so the epilogue of a tile overlaps the next tile's MMAs.
     static constexpr int HALVES = kWide ? 2 : 1;
     static constexpr int BM = 128 * HALVES;
-    static constexpr int BN = 256;
+    static constexpr int BN = kBN;                   // 256, or 224 (K-major B only)
     static constexpr int ES = kTF32 ? 4 : 2;        // bytes per input element
     static constexpr int BK = 128 / ES;             // elements of K per stage (128 bytes)
     static constexpr int UK = 32 / ES;              // elements of K per MMA (32 bytes)
@@ -58,11 +62,14 @@ struct Cfg {
     static constexpr uint32_t A_BYTES = BM * 128;
     static constexpr uint32_t B_BYTES = NCH * CH_BYTES;
     static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t TCOL = 256;           // tensor-memory columns between accumulators / halves
     static constexpr int GROUP_M = kWide ? 8 : 16;
     static constexpr uint32_t IDESC =
         instr_desc(kTF32 ? kFormatTF32 : kFormatBF16, 0, kBKMajor ? 0u : 1u, 128, BN);
     static constexpr size_t SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + (2 * STAGES + 4) * 8 + 16;
-    static_assert(ACCS * HALVES * BN <= 512, "accumulators exceed tensor memory");
+    static_assert(ACCS * HALVES * 256 <= 512, "accumulators exceed tensor memory");
+    static_assert(BN % 32 == 0 && BN <= 256, "tile width");
+    static_assert(kBKMajor || BN % CH == 0, "an N-contiguous B tile is a whole number of 128-byte chunks");
 };
 
 constexpr int kThreads = 192;
@@ -78,11 +85,22 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
     tn = in_group / rows;
 }
 
-template <bool kTF32, bool kBKMajor, bool kWide>
+// Named barrier of the four epilogue warps (threads 64 .. 191).
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// The CTAs walk the persistent plan of stream_k.cuh: whole tiles b, b + G, ...
+// and, when `ws` is given and the last wave would be partial, a stream-K
+// region whose tiles may be split along k between two CTAs.  The tail of a
+// split tile stores its fp32 accumulator in its CTA's `ws` slot and raises
+// its flag; the head waits for the flag, adds that partial to its own
+// accumulator (always head + tail) and stores the tile.  Split tiles need
+// every CTA resident: the launch is cooperative.
+template <bool kTF32, bool kBKMajor, bool kWide, int kBN, bool kSK>
 __global__ void __launch_bounds__(kThreads, 1)
 umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-            float* __restrict__ C, int64_t ldc, int M, int N, int K, int vec_store, uint32_t* status) {
-    using G = Cfg<kTF32, kBKMajor, kWide>;
+            float* __restrict__ C, int64_t ldc, int M, int N, int K, int vec_store, uint32_t* status,
+            float* __restrict__ ws, unsigned* __restrict__ flags) {
+    using G = Cfg<kTF32, kBKMajor, kWide, kBN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -93,13 +111,35 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     uint64_t* acc_full = empty + G::STAGES;    // [2]
     uint64_t* acc_empty = acc_full + 2;        // [2]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+    __shared__ int s_flag_ok;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int tiles_m = (M + G::BM - 1) / G::BM;
     const int tiles_n = (N + G::BN - 1) / G::BN;
-    const int tiles = tiles_m * tiles_n;
     const int KT = (K + G::BK - 1) / G::BK;
+    const int tiles = tiles_m * tiles_n;
+    SkPlan plan;
+    if (kSK) plan.init(tiles, KT, blockIdx.x, gridDim.x);
+    // The CTA's segments (tile, k-phases [ka, kz)): with kSK the plan's
+    // sequence, otherwise whole tiles b, b + G, ...  Each role walks its own.
+    struct Seq {
+        SkCursor cur;
+        int t_next;
+    };
+    auto seq_init = [&](Seq& q) {
+        q.t_next = blockIdx.x;
+        if (kSK) q.cur.init(plan);
+    };
+    auto seq_next = [&](Seq& q, int& t, int& ka, int& kz) -> bool {
+        if (kSK) return q.cur.next(plan, KT, t, ka, kz);
+        if (q.t_next >= tiles) return false;
+        t = q.t_next;
+        q.t_next += gridDim.x;
+        ka = 0;
+        kz = KT;
+        return true;
+    };
 
     if (threadIdx.x == 0) {
         tma_prefetch_map(&tmA);
@@ -126,10 +166,13 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x) {
+            Seq sq;
+            seq_init(sq);
+            int tile, ka, kz;
+            while (ok && seq_next(sq, tile, ka, kz)) {
                 int tm, tn;
                 tile_coords(tile, tiles_m, tiles_n, G::GROUP_M, tm, tn);
-                for (int kb = 0; kb < KT; ++kb) {
+                for (int kb = ka; kb < kz; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, status)) { ok = false; break; }
                     mbar_arrive_expect_tx(&full[s], G::A_BYTES + G::B_BYTES);
                     tma_load_2d(sA + s * G::A_BYTES, &tmA, &full[s], kb * G::BK, tm * G::BM);
@@ -153,13 +196,16 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             uint32_t ph = 0;
             bool ok = true;
             int it = 0;
-            for (int tile = blockIdx.x; ok && tile < tiles; tile += gridDim.x, ++it) {
+            Seq sq;
+            seq_init(sq);
+            int tile, ka, kz;
+            for (; ok && seq_next(sq, tile, ka, kz); ++it) {
                 const uint32_t acc = it % G::ACCS;
                 const uint32_t acc_ph = (it / G::ACCS) & 1;
                 if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1u, status)) break;
                 tc_fence_after_sync();
-                const uint32_t d_tmem = tmem_base + acc * (G::HALVES * G::BN);
-                for (int kb = 0; kb < KT; ++kb) {
+                const uint32_t d_tmem = tmem_base + acc * (G::HALVES * G::TCOL);
+                for (int kb = ka; kb < kz; ++kb) {
                     if (!mbar_wait(&full[s], ph, status)) { ok = false; break; }
                     tc_fence_after_sync();
                     const uint32_t a0 = smem_addr(sA + s * G::A_BYTES);
@@ -177,10 +223,12 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                             // A: K-major, 128-byte rows, 8-row swizzle atoms 1 KiB apart;
                             //    rows 128h.. start 16 KiB in; slice kk starts 32*kk bytes in.
                             const uint64_t ad = smem_desc(a0 + h * 128 * 128 + kk * 32, 16, 1024, kSwizzle128B);
+                            // The segment's first MMA overwrites the accumulator.
+                            const bool accumulate = kb != ka || kk != 0;
                             if (kTF32)
-                                umma_tf32(d_tmem + h * G::BN, ad, bd, G::IDESC, (kb | kk) != 0);
+                                umma_tf32(d_tmem + h * G::TCOL, ad, bd, G::IDESC, accumulate);
                             else
-                                umma_f16(d_tmem + h * G::BN, ad, bd, G::IDESC, (kb | kk) != 0);
+                                umma_f16(d_tmem + h * G::TCOL, ad, bd, G::IDESC, accumulate);
                         }
                     }
                     umma_commit(&empty[s]);   // stage free once these MMAs complete
@@ -192,27 +240,66 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
     } else {
         // --------------------------------------------------- epilogue --
+        // A warp whose wait ran out keeps the others' control flow (it stops
+        // waiting but still reaches every epilogue_sync), so none is left
+        // waiting at a named barrier.
         const int quarter = warp & 3;   // tensor-memory lanes 32*quarter .. +31
+        const int row_in_half = quarter * 32 + lane;
+        bool ok = true;
         int it = 0;
-        for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++it) {
+        Seq sq;
+        seq_init(sq);
+        int tile, ka, kz;
+        for (; seq_next(sq, tile, ka, kz); ++it) {
             const uint32_t acc = it % G::ACCS;
             const uint32_t acc_ph = (it / G::ACCS) & 1;
-            if (!mbar_wait(&acc_full[acc], acc_ph, status)) break;
+            if (ok && !mbar_wait(&acc_full[acc], acc_ph, status)) ok = false;
             tc_fence_after_sync();
             __syncwarp();   // tcgen05.ld below is warp-collective
             int tm, tn;
             tile_coords(tile, tiles_m, tiles_n, G::GROUP_M, tm, tn);
+            const bool tail = kSK && ka > 0;
+            const bool head = kSK && !tail && kz < KT;
+            // Partial tile of a CTA's slot: float4 ((h * BN/32 + c) * 8 + q) * 128 + row
+            // holds columns 32c + 4q .. +3 of row `row` of half h, so a warp
+            // stores or loads 512 contiguous bytes.
+            float4* my_part = reinterpret_cast<float4*>(ws + static_cast<int64_t>(blockIdx.x) * G::BM * G::BN);
+            const float4* next_part =
+                reinterpret_cast<const float4*>(ws + static_cast<int64_t>(blockIdx.x + 1) * G::BM * G::BN);
+            if (head) {
+                if (threadIdx.x == 64) s_flag_ok = ok && wait_flag(flags + blockIdx.x + 1, status) ? 1 : 0;
+                epilogue_sync();
+            }
 #pragma unroll
             for (int h = 0; h < G::HALVES; ++h) {
-                const int row = tm * G::BM + h * 128 + quarter * 32 + lane;
+                const int row = tm * G::BM + h * 128 + row_in_half;
                 float* crow = C + static_cast<int64_t>(row) * ldc;
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       (acc * G::HALVES + h) * G::BN;
+                                       (acc * G::HALVES + h) * G::TCOL;
 #pragma unroll 1
                 for (int c = 0; c < G::BN / 32; ++c) {
                     uint32_t r[32];
                     tmem_load_32(t_row + c * 32, r);
                     tmem_load_wait();
+                    const int slot = (h * (G::BN / 32) + c) * 8;
+                    if (tail) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            my_part[(slot + q) * 128 + row_in_half] =
+                                make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                            __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                        continue;
+                    }
+                    if (head && s_flag_ok) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 v = __ldcg(next_part + (slot + q) * 128 + row_in_half);
+                            r[4 * q] = __float_as_uint(__uint_as_float(r[4 * q]) + v.x);
+                            r[4 * q + 1] = __float_as_uint(__uint_as_float(r[4 * q + 1]) + v.y);
+                            r[4 * q + 2] = __float_as_uint(__uint_as_float(r[4 * q + 2]) + v.z);
+                            r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + v.w);
+                        }
+                    }
                     const int col0 = tn * G::BN + c * 32;
                     if (row < M) {
                         if (vec_store && col0 + 32 <= N) {
@@ -231,6 +318,11 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             }
             tc_fence_before_sync();
             mbar_arrive(&acc_empty[acc]);
+            if (tail) {
+                __threadfence();
+                epilogue_sync();
+                if (threadIdx.x == 64) st_release_u32(flags + blockIdx.x, 1u);
+            }
         }
     }
 
@@ -242,9 +334,40 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
 }
 
-template <bool kTF32, bool kBKMajor, bool kWide>
-cudaError_t launch(const Problem& p, const Device& dev) {
-    using G = Cfg<kTF32, kBKMajor, kWide>;
+template <bool kTF32, bool kBKMajor, bool kWide, int kBN>
+int64_t tile_count(const Problem& p) {
+    using G = Cfg<kTF32, kBKMajor, kWide, kBN>;
+    return static_cast<int64_t>((p.m + G::BM - 1) / G::BM) * ((p.n + G::BN - 1) / G::BN);
+}
+
+// Stream-K when the plan has a region and the whole-tile grid would fill
+// less than 3/4 of its CTA slots.  Measured on GB300 (TFLOP/s, whole tiles ->
+// stream-K): 3300 x 3000 x 3100 TF32 354 -> 479, bf16 477 -> 559 (51 %
+// filled); 2000 x 2600 x 1000 TF32 219 -> 228 (58 %); but 4096^3 TF32 685 ->
+// 649 (84 %) and 8192^3 bf16 1802 -> 1603 (96 %): the runs start at scattered
+// k, so the region's A and B are live in L2 all at once (ncu: DRAM reads
+// 0.87 -> 1.92 GB, L2 hit rate 77 -> 62 %), whereas whole tiles step through
+// k together.
+template <bool kTF32, bool kBKMajor, bool kWide, int kBN>
+bool has_sk(const Problem& p, const Device& dev) {
+    using G = Cfg<kTF32, kBKMajor, kWide, kBN>;
+    const int64_t tiles = tile_count<kTF32, kBKMajor, kWide, kBN>(p);
+    const int64_t waves = (tiles + dev.sm_count - 1) / dev.sm_count;
+    return sk_has_region(tiles, (p.k + G::BK - 1) / G::BK, dev.sm_count) && 4 * tiles < 3 * waves * dev.sm_count;
+}
+
+template <bool kTF32, bool kBKMajor, bool kWide, int kBN>
+uint64_t workspace_bytes(const Problem& p, const Device& dev) {
+    using G = Cfg<kTF32, kBKMajor, kWide, kBN>;
+    if (!has_sk<kTF32, kBKMajor, kWide, kBN>(p, dev)) return 0;
+    return static_cast<uint64_t>(dev.sm_count) * (static_cast<uint64_t>(G::BM) * G::BN * sizeof(float) +
+                                                  sizeof(unsigned));
+}
+
+// Stream-K (kSK, with its workspace) or whole tiles.
+template <bool kTF32, bool kBKMajor, bool kWide, int kBN, bool kSK>
+cudaError_t launch(const Problem& p, const Device& dev, void* workspace) {
+    using G = Cfg<kTF32, kBKMajor, kWide, kBN>;
     const CUtensorMapDataType dt = kTF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap ta, tb;
     const bool b_ok =
@@ -252,21 +375,53 @@ cudaError_t launch(const Problem& p, const Device& dev) {
                  : make_tensor_map(&tb, dt, G::ES, p.B, p.k, p.n, p.ldb, G::BK, G::CH, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!make_tensor_map(&ta, dt, G::ES, p.A, p.m, p.k, p.lda, G::BM, G::BK, CU_TENSOR_MAP_SWIZZLE_128B) || !b_ok)
         return cudaErrorInvalidValue;
-    auto kernel = umma_kernel<kTF32, kBKMajor, kWide>;
+    auto kernel = umma_kernel<kTF32, kBKMajor, kWide, kBN, kSK>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(G::SMEM));
     if (err != cudaSuccess) {
         set_error("cudaFuncSetAttribute(umma_kernel): %s", cudaGetErrorString(err));
         return err;
     }
-    const int64_t tiles = static_cast<int64_t>((p.m + G::BM - 1) / G::BM) * ((p.n + G::BN - 1) / G::BN);
-    const int grid = static_cast<int>(tiles < dev.sm_count ? tiles : dev.sm_count);
+    const int64_t tiles = tile_count<kTF32, kBKMajor, kWide, kBN>(p);
     const int vec_store = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
-    kernel<<<grid, kThreads, G::SMEM, p.stream>>>(ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status);
+    float* ws = nullptr;
+    unsigned* flags = nullptr;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = G::SMEM;
+    cfg.stream = p.stream;
+    cfg.gridDim = dim3(static_cast<unsigned>(tiles < dev.sm_count ? tiles : dev.sm_count), 1, 1);
+    if (kSK) {
+        if (!workspace) {
+            set_error("umma_kernel: stream-K form launched without its workspace");
+            return cudaErrorInvalidValue;
+        }
+        // one partial tile and one flag per CTA; the flags start cleared
+        ws = static_cast<float*>(workspace);
+        flags = reinterpret_cast<unsigned*>(ws + static_cast<size_t>(dev.sm_count) * G::BM * G::BN);
+        err = cudaMemsetAsync(flags, 0, dev.sm_count * sizeof(unsigned), p.stream);
+        if (err != cudaSuccess) {
+            set_error("stream-K flags: %s", cudaGetErrorString(err));
+            return err;
+        }
+        attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: a head may wait for its tail
+        attr[0].val.cooperative = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count), 1, 1);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    err = cudaLaunchKernelEx(&cfg, kernel, ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status, ws, flags);
     count_launch();
-    err = cudaGetLastError();
     if (err != cudaSuccess) set_error("umma_kernel launch: %s", cudaGetErrorString(err));
     return err;
+}
+
+template <bool kTF32, bool kBKMajor, bool kWide, int kBN>
+cudaError_t launch_any(const Problem& p, const Device& dev, void* workspace) {
+    if (workspace && has_sk<kTF32, kBKMajor, kWide, kBN>(p, dev))
+        return launch<kTF32, kBKMajor, kWide, kBN, true>(p, dev, workspace);
+    return launch<kTF32, kBKMajor, kWide, kBN, false>(p, dev, nullptr);
 }
 
 }  // namespace
@@ -278,10 +433,46 @@ cudaError_t launch(const Problem& p, const Device& dev) {
 // 8192 x 8192 x 2048 1235 vs 1346: long k favours the wide tiles.
 constexpr int kWideMinK = 3072;
 
-cudaError_t launch_umma(const Problem& p, const Device& dev, bool tf32) {
+// Tile width of the TF32 kernels: 224 instead of 256 when 256-wide tiles
+// would not take stream-K and 224-wide ones fill the occupied CTA slots
+// better by more than 2 % (both are legal tcgen05 N for M = 128; the K-major
+// B tile has no 128-byte-chunk constraint along N).  The filled fraction of
+// the slots is also the time ratio: time ~ slots x tile area.  Measured on
+// GB300 (TFLOP/s, 256 -> 224): 4096^3 679 -> 714 (304 tiles = 2 full waves,
+// 96 % filled, against 84 %); 2048 x 2048 x 8192 377 -> 392.  With
+// stream-K the wider tile is better (3300 x 3000 x 3100: 479 against 411).
+bool tf32_narrow_n(const Problem& p, const Device& dev) {
     const bool wide = p.k >= kWideMinK;
-    if (tf32) return wide ? launch<true, true, true>(p, dev) : launch<true, true, false>(p, dev);
-    return wide ? launch<false, false, true>(p, dev) : launch<false, false, false>(p, dev);
+    if (wide ? has_sk<true, true, true, 256>(p, dev) : has_sk<true, true, false, 256>(p, dev)) return false;
+    const int64_t bm = wide ? 256 : 128, G = dev.sm_count;
+    auto fill = [&](int64_t bn) {
+        const int64_t tiles = ((p.m + bm - 1) / bm) * ((p.n + bn - 1) / bn);
+        const int64_t slots = (tiles + G - 1) / G * G;
+        return static_cast<double>(p.m) * p.n / (static_cast<double>(slots) * bm * bn);
+    };
+    return fill(224) > 1.02 * fill(256);
+}
+
+uint64_t umma_workspace_bytes(const Problem& p, const Device& dev, bool tf32) {
+    const bool wide = p.k >= kWideMinK;
+    if (tf32) {
+        if (tf32_narrow_n(p, dev)) return 0;   // 224-wide tiles: whole tiles only
+        return wide ? workspace_bytes<true, true, true, 256>(p, dev) : workspace_bytes<true, true, false, 256>(p, dev);
+    }
+    return wide ? workspace_bytes<false, false, true, 256>(p, dev) : workspace_bytes<false, false, false, 256>(p, dev);
+}
+
+cudaError_t launch_umma(const Problem& p, const Device& dev, bool tf32, void* workspace) {
+    const bool wide = p.k >= kWideMinK;
+    if (tf32) {
+        if (tf32_narrow_n(p, dev))
+            return wide ? launch<true, true, true, 224, false>(p, dev, nullptr)
+                        : launch<true, true, false, 224, false>(p, dev, nullptr);
+        return wide ? launch_any<true, true, true, 256>(p, dev, workspace)
+                    : launch_any<true, true, false, 256>(p, dev, workspace);
+    }
+    return wide ? launch_any<false, false, true, 256>(p, dev, workspace)
+                : launch_any<false, false, false, 256>(p, dev, workspace);
 }
 
 }  // namespace tgemm

@@ -88,6 +88,24 @@ def test_fp32_persistent_schedule(shape):
     assert torch.equal(parity.ENTRY["f32"](A, B), parity.ENTRY["f32"](A, B))
 
 
+# Tensor-core shapes whose last partial wave of tiles is split along k between
+# two CTAs (stream-K): wide 256 x 256 tiles with no whole-tile round, narrow
+# 128 x 256 tiles, wide tiles after one round.  Ragged, whole output checked.
+UMMA_SK_SHAPES = [(3300, 3000, 3100), (2000, 2600, 1000), (2600, 4000, 4100)]
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+@pytest.mark.parametrize("shape", UMMA_SK_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_tensor_core_split_tiles(mode, shape):
+    m, n, k = shape
+    parity.full_check(mode, inputs.random_case(9000 + m + n + k, m, n, k, kind="int"), f"{mode} int {shape}")
+    case = inputs.random_case(9500 + m + n + k, m, n, k, kind="uniform")
+    parity.full_check(mode, case, f"{mode} uniform {shape}")
+    A, B = parity.inputs_for(mode, case)
+    A, B = parity.to_device(A), parity.to_device(B)
+    assert torch.equal(parity.ENTRY[mode](A, B), parity.ENTRY[mode](A, B))
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_leading_dimensions_and_untouched_padding(mode):
     m, n, k = 200, 150, 90

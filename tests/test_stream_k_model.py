@@ -161,3 +161,54 @@ def test_head_plus_tail_is_the_full_sum_on_integers():
                 C[r0:r0 + BM, c0:c0 + BN] = part
     assert not np.isnan(C).any()
     np.testing.assert_array_equal(C, A @ B)
+
+
+# ---- tcgen05 kernels (csrc/umma.cu): tile width, then the same plan ----
+def umma_choice(m, n, k, mode, G=152):
+    """(tile width, tiles, KT, stream-K) the launcher picks: 256 x BN tiles when
+    k >= 3072, else 128 x BN.  Stream-K (always with BN = 256) when the plan
+    has a region and whole tiles would fill less than 3/4 of the occupied CTA
+    slots; otherwise TF32 takes BN = 224 when that fills them better by more
+    than 2 %."""
+    bm = 256 if k >= 3072 else 128
+    kt = -(-k // (32 if mode == "tf32" else 64))
+
+    def fill(bn):
+        tiles = -(-m // bm) * -(-n // bn)
+        return m * n / (-(-tiles // G) * G * bm * bn), tiles
+
+    tiles = fill(256)[1]
+    waves = -(-tiles // G)
+    r = tiles % G
+    if tiles >= G and r > 0 and r * kt >= G and 4 * tiles < 3 * waves * G:
+        return 256, tiles, kt, True
+    bn = 224 if mode == "tf32" and fill(224)[0] > 1.02 * fill(256)[0] else 256
+    return bn, fill(bn)[1], kt, False
+
+
+def test_umma_choices_on_the_benchmarked_shapes():
+    assert umma_choice(4096, 4096, 4096, "tf32") == (224, 304, 128, False)   # 2 full waves
+    assert umma_choice(8192, 8192, 8192, "bf16")[::3] == (256, False)        # 1024 tiles: 96 % filled
+    assert umma_choice(4097, 3001, 1023, "tf32")[0] == 256
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+def test_umma_stream_k_shapes(mode):
+    G = 152
+    # the GPU parity shapes for the split path: wide with no whole-tile round,
+    # narrow, wide with a round
+    for shape in [(3300, 3000, 3100), (2000, 2600, 1000), (2600, 4000, 4100)]:
+        bn, tiles, kt, sk = umma_choice(*shape, mode)
+        assert sk, shape
+        per_cta = []
+        for b in range(G):
+            n_dp, t_sk0, v, v1 = plan(tiles, kt, b, G)
+            segs = [(b + j * G, 0, kt) for j in range(n_dp)]
+            while v < v1:
+                q, ka = divmod(v, kt)
+                kz = min(kt, ka + (v1 - v))
+                segs.append((t_sk0 + q, ka, kz))
+                v += kz - ka
+            per_cta.append(segs)
+        assert sum(roles(s, kt).count("head") for s in per_cta) > 20
+    assert not umma_choice(1024, 1024, 1024, mode)[3]   # fewer tiles than SMs
