@@ -31,13 +31,19 @@
 //    tile rows; the epilogue writes 4 rows x 128 contiguous bytes per warp
 //    instruction with 128-bit stores.
 //
+//  * The last wave.  With T = q G + r tiles on G SMs (r < 0.9 G), the one-tile
+//    grid runs the q G tiles of the full rounds and the r tiles left are cut
+//    along k into `parts` pieces that fill whole rounds best; each piece's
+//    partial sums go to a workspace slot and a reduce kernel adds a tile's
+//    pieces in part order.
+//
 // Each C element is the sum over k, in ascending k, of fused multiply-adds
-// into one fp32 register that starts at 0, then stored once.
+// into one fp32 register that starts at 0 (for a split tile: per piece, then
+// the pieces added in order), then stored once.
 #include <cstdio>
 
 #include "device.cuh"
 #include "host.h"
-#include "stream_k.cuh"
 
 namespace tgemm {
 namespace {
@@ -242,60 +248,35 @@ ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     store_tile(acc, C, ldc, M, N, m0, n0, a_row0, b_col0, vec_store);
 }
 
-// Persistent form: one CTA per SM walking its SkPlan sequence; the copy
-// pipeline runs on from one segment into the next.  A tile shared by two
-// CTAs is finished by the one holding its first phases (the head): the other
-// (the tail) writes its partial sums to `ws` and raises its flag, and the C
-// value is (head partial) + (tail partial), always in that order.  The launch
-// is cooperative, so every CTA is resident and a head's wait for its tail
-// ends.
+// Remainder tiles cut along k ("split-K"): block u computes part u % parts of
+// tile tile0 + u / parts -- k-phases [KT part / parts, KT (part + 1) / parts)
+// -- with the data-parallel kernel's pipeline and stores its partial sums in
+// slot u of `ws` (float4 j of thread t at j * THREADS + t, so a warp stores
+// 512 contiguous bytes).
 __global__ void __launch_bounds__(FCfg<4>::THREADS, 1)
-ffma_f32_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   float* __restrict__ C, int64_t ldc, int M, int N, int K, int vec_store, uint32_t* status,
-                   float* __restrict__ ws, unsigned* __restrict__ flags) {
+ffma_f32_split_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      float* __restrict__ ws, int M, int N, int K, int tile0, int parts, uint32_t* status) {
     using F = FCfg<4>;
     constexpr int kBM = F::BM;
     extern __shared__ uint8_t smem_raw[];
     const Smem<4> sm(smem_raw);
-    __shared__ int s_flag_ok;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int tiles_m = (M + kBM - 1) / kBM;
-    const int tiles_n = (N + kBN - 1) / kBN;
+    const int u = blockIdx.x, part = u % parts;
+    int tile_m, tile_n;
+    tile_coords(tile0 + u / parts, (M + kBM - 1) / kBM, (N + kBN - 1) / kBN, tile_m, tile_n);
+    const int m0 = tile_m * kBM;
+    const int n0 = tile_n * kBN;
     const int KT = (K + kBK - 1) / kBK;
-    // The plan and the producer's cursor are read once per segment, so they
-    // live in shared memory rather than in registers through the k loop.
-    __shared__ SkPlan s_plan;
-    __shared__ SkCursor s_pc;
-    int NI;
-    {
-        SkPlan plan;
-        plan.init(tiles_m * tiles_n, KT, blockIdx.x, gridDim.x);
-        NI = plan.iterations(KT);
-        if (tid == 0) {
-            s_plan = plan;
-            s_pc.init(plan);
-        }
-    }
+    const int k0 = static_cast<int>(static_cast<int64_t>(KT) * part / parts);
+    const int NI = static_cast<int>(static_cast<int64_t>(KT) * (part + 1) / parts) - k0;
 
-    // Producer (thread 0): its own cursor, up to kStages iterations ahead of
-    // the consumers'; the tile origin is recomputed once per segment.
-    int p_kb = 0, p_kz = 0, p_m0 = 0, p_n0 = 0;
-    auto issue_next = [&](int slot) {
-        if (p_kb == p_kz) {
-            int t;
-            s_pc.next(s_plan, KT, t, p_kb, p_kz);
-            int tm_, tn_;
-            tile_coords(t, tiles_m, tiles_n, tm_, tn_);
-            p_m0 = tm_ * kBM;
-            p_n0 = tn_ * kBN;
-        }
+    auto issue = [&](int slot, int i) {
         mbar_arrive_expect_tx(&sm.full[slot], F::STAGE_A + kStageB);
-        tma_load_2d(sm.sA + slot * (kBM * kBK), &tmA, &sm.full[slot], p_kb * kBK, p_m0);
-        tma_load_2d(sm.sB + slot * (kBK * kBN), &tmB, &sm.full[slot], p_n0, p_kb * kBK);
-        ++p_kb;
+        tma_load_2d(sm.sA + slot * (kBM * kBK), &tmA, &sm.full[slot], (k0 + i) * kBK, m0);
+        tma_load_2d(sm.sB + slot * (kBK * kBN), &tmB, &sm.full[slot], n0, (k0 + i) * kBK);
     };
     if (tid == 0) {
         tma_prefetch_map(&tmA);
@@ -308,7 +289,7 @@ ffma_f32_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
     __syncthreads();
     if (tid == 0)
-        for (int s = 0; s < min(NI, kStages); ++s) issue_next(s);
+        for (int s = 0; s < min(NI, kStages); ++s) issue(s, s);
 
     // Thread layout and swizzle as in the data-parallel kernel.
     const int wm = warp >> 1, wn = warp & 1;
@@ -317,84 +298,72 @@ ffma_f32_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const int b_col0 = 64 * wn + 4 * tn;
     const int swz_even = kBK == 16 ? (tm >> 1) : tm;
 
+    Acc acc;
+    zero(acc);
     bool ok = true;
     int s = 0;
     uint32_t phase = 0;
-    int it = 0;                                   // iterations consumed so far
-    SkCursor cc;
-    cc.init(s_plan);
-    int t, ka, kz;
-    while (cc.next(s_plan, KT, t, ka, kz)) {
-        const int seg_end = it + (kz - ka);
-        Acc acc;
-        zero(acc);
-        for (; it < seg_end; ++it) {
-            // Refill the stage drained in the previous iteration with iteration
-            // it-1+kStages.  A thread whose wait ran out stops waiting (and
-            // issuing) but keeps the others' control flow, so every
-            // __syncthreads below is reached.
-            if (tid == 0 && it > 0) {
-                const int next = it - 1 + kStages;
-                if (next < NI && ok) {
-                    const int ps = (it - 1) % kStages;
-                    const uint32_t pph = static_cast<uint32_t>((it - 1) / kStages) & 1u;
-                    if (mbar_wait(&sm.empty[ps], pph, status)) issue_next(ps);
-                    else ok = false;
-                }
-            }
-            if (!mbar_try_wait(smem_addr(&sm.full[s]), phase) && ok) ok = mbar_wait(&sm.full[s], phase, status);
-            fma_phase(acc, sm.sA + s * (kBM * kBK), sm.sB + s * (kBK * kBN), a_row0, b_col0, swz_even);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.empty[s]);
-            if (++s == kStages) { s = 0; phase ^= 1u; }
-        }
-
-        int tile_m, tile_n;
-        tile_coords(t, tiles_m, tiles_n, tile_m, tile_n);
-        if (ka > 0) {
-            // Tail: hand the 64 partial sums of each thread to the previous CTA.
-            // float4 j of thread tid goes to j * THREADS + tid, so a warp stores
-            // 512 contiguous bytes.
-            float4* dst = reinterpret_cast<float4*>(ws + static_cast<int64_t>(blockIdx.x) * kBM * kBN) + tid;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-#pragma unroll
-                for (int p = 0; p < 4; p += 2)
-                    dst[(i * 2 + p / 2) * F::THREADS] =
-                        make_float4(acc[i][p].x, acc[i][p].y, acc[i][p + 1].x, acc[i][p + 1].y);
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) st_release_u32(flags + blockIdx.x, 1u);
-            continue;
-        }
-        if (kz < KT) {
-            // Head: wait for the next CTA's tail of this tile and add it.
-            if (tid == 0) s_flag_ok = ok && wait_flag(flags + blockIdx.x + 1, status) ? 1 : 0;
-            __syncthreads();
-            if (s_flag_ok) {
-                const float4* src =
-                    reinterpret_cast<const float4*>(ws + static_cast<int64_t>(blockIdx.x + 1) * kBM * kBN) + tid;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-#pragma unroll
-                    for (int p = 0; p < 4; p += 2) {
-                        const float4 v = __ldcg(src + (i * 2 + p / 2) * F::THREADS);
-                        acc[i][p].x += v.x;
-                        acc[i][p].y += v.y;
-                        acc[i][p + 1].x += v.z;
-                        acc[i][p + 1].y += v.w;
-                    }
+    for (int i = 0; i < NI; ++i) {
+        if (tid == 0 && i > 0) {
+            const int next = i - 1 + kStages;
+            if (next < NI) {
+                const int ps = (i - 1) % kStages;
+                const uint32_t pph = static_cast<uint32_t>((i - 1) / kStages) & 1u;
+                if (!mbar_wait(&sm.empty[ps], pph, status)) { ok = false; break; }
+                issue(ps, next);
             }
         }
-        store_tile(acc, C, ldc, M, N, tile_m * kBM, tile_n * kBN, a_row0, b_col0, vec_store);
+        if (!mbar_wait(&sm.full[s], phase, status)) { ok = false; break; }
+        fma_phase(acc, sm.sA + s * (kBM * kBK), sm.sB + s * (kBK * kBN), a_row0, b_col0, swz_even);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[s]);
+        if (++s == kStages) { s = 0; phase ^= 1u; }
     }
-    (void)ok;   // on a timeout the status word records it and C is incomplete
+    if (!ok) return;   // status records the timeout
+    float4* dst = reinterpret_cast<float4*>(ws + static_cast<int64_t>(u) * kBM * kBN) + tid;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int p = 0; p < 4; p += 2)
+            dst[(i * 2 + p / 2) * F::THREADS] = make_float4(acc[i][p].x, acc[i][p].y, acc[i][p + 1].x, acc[i][p + 1].y);
 }
 
-// Launches the data-parallel kernel (workspace == nullptr) or, with its
-// workspace, the stream-K kernel (WR = 4).
+// C of the remainder tiles: tile tile0 + b is the sum of the split kernel's
+// slots b * parts .. b * parts + parts - 1, added in part order.
+__global__ void __launch_bounds__(FCfg<4>::THREADS)
+ffma_f32_reduce_kernel(const float* __restrict__ ws, float* __restrict__ C, int64_t ldc, int M, int N, int tile0,
+                       int parts, int vec_store) {
+    using F = FCfg<4>;
+    constexpr int kBM = F::BM;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wm = warp >> 1, wn = warp & 1;
+    const int tm = lane >> 3, tn = lane & 7;
+    const int a_row0 = 32 * wm + tm;
+    const int b_col0 = 64 * wn + 4 * tn;
+    int tile_m, tile_n;
+    tile_coords(tile0 + blockIdx.x, (M + kBM - 1) / kBM, (N + kBN - 1) / kBN, tile_m, tile_n);
+    Acc acc;
+    zero(acc);
+    const float4* src = reinterpret_cast<const float4*>(ws + static_cast<int64_t>(blockIdx.x) * parts * kBM * kBN) + tid;
+    for (int q = 0; q < parts; ++q) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int p = 0; p < 4; p += 2) {
+                const float4 v = __ldcs(src + (i * 2 + p / 2) * F::THREADS);
+                acc[i][p].x += v.x;
+                acc[i][p].y += v.y;
+                acc[i][p + 1].x += v.z;
+                acc[i][p + 1].y += v.w;
+            }
+        src += kBM * kBN / 4;
+    }
+    store_tile(acc, C, ldc, M, N, tile_m * kBM, tile_n * kBN, a_row0, b_col0, vec_store);
+}
+
+// Launches the one-tile-per-CTA kernel over all tiles.
 template <int WR>
-cudaError_t launch_wr(const Problem& p, const Device& dev, void* workspace) {
+cudaError_t launch_wr(const Problem& p, const Device& dev) {
     using F = FCfg<WR>;
     CUtensorMap ta, tb;
     if (!make_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.A, p.m, p.k, p.lda, F::BM, kBK,
@@ -402,46 +371,19 @@ cudaError_t launch_wr(const Problem& p, const Device& dev, void* workspace) {
         !make_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.k, p.n, p.ldb, kBK, kBN,
                          CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    const bool sk = workspace != nullptr;
-    const void* kernel = sk ? reinterpret_cast<const void*>(ffma_f32_sk_kernel)
-                            : reinterpret_cast<const void*>(ffma_f32_kernel<WR>);
-    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(ffma_f32_kernel<WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(F::SMEM));
     if (err != cudaSuccess) {
-        set_error("cudaFuncSetAttribute(ffma_f32 kernel): %s", cudaGetErrorString(err));
+        set_error("cudaFuncSetAttribute(ffma_f32_kernel): %s", cudaGetErrorString(err));
         return err;
     }
     const int64_t tiles = static_cast<int64_t>((p.m + F::BM - 1) / F::BM) * ((p.n + kBN - 1) / kBN);
     const int vec_store = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(F::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = F::SMEM;
-    cfg.stream = p.stream;
-    if (!sk) {
-        cfg.gridDim = dim3(static_cast<unsigned>(tiles), 1, 1);
-        err = cudaLaunchKernelEx(&cfg, ffma_f32_kernel<WR>, ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store,
-                                 dev.status);
-    } else {
-        // one partial tile and one flag per CTA; the flags start cleared
-        const unsigned grid = static_cast<unsigned>(dev.sm_count);
-        float* ws = static_cast<float*>(workspace);
-        unsigned* flags = reinterpret_cast<unsigned*>(ws + static_cast<size_t>(grid) * F::BM * kBN);
-        err = cudaMemsetAsync(flags, 0, grid * sizeof(unsigned), p.stream);
-        if (err != cudaSuccess) {
-            set_error("stream-K flags: %s", cudaGetErrorString(err));
-            return err;
-        }
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: a head may wait for its tail
-        attr[0].val.cooperative = 1;
-        cfg.gridDim = dim3(grid, 1, 1);
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        err = cudaLaunchKernelEx(&cfg, ffma_f32_sk_kernel, ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store,
-                                 dev.status, ws, flags);
-    }
+    ffma_f32_kernel<WR><<<static_cast<unsigned>(tiles), F::THREADS, F::SMEM, p.stream>>>(
+        ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status);
     count_launch();
-    if (err != cudaSuccess) set_error("ffma_f32 kernel launch: %s", cudaGetErrorString(err));
+    err = cudaGetLastError();
+    if (err != cudaSuccess) set_error("ffma_f32_kernel launch: %s", cudaGetErrorString(err));
     return err;
 }
 
@@ -449,39 +391,95 @@ cudaError_t launch_wr(const Problem& p, const Device& dev, void* workspace) {
 // 64-row CTAs per SM; 4097 x 3001 x 1024 42.8 vs 46.3.
 constexpr int kShortK = 2048;
 
-// The persistent kernel when k is long, the one-tile-per-CTA grid would
-// leave at least a tenth of its CTA slots empty (tiles / (waves * G) < 0.9),
-// and the plan has a stream-K region (same rule as SkPlan).  Measured on
-// GB300 (TFLOP/s, one-tile grid -> persistent): 2500 x 2000 x 2300 (2.1
-// waves) 37.6 -> 48.7; 2000 x 2000 x 4096 (1.7 waves) 43.6 -> 46.7; but
-// 4096^3 (6.7 waves) 53.1 -> 50.7 and 3000 x 6000 x 4096 (7.4 waves)
-// 50.5 -> 49.4, where the one-tile grid's loop runs faster.
-bool use_stream_k(const Problem& p, const Device& dev) {
+// Split remainder: the one-tile grid runs the q G tiles of the full rounds;
+// the r tiles left (r < 0.9 G) are cut along k into `parts` pieces, chosen
+// so that r * parts pieces fill whole rounds of the grid best (each round of
+// pieces takes 1/parts of a tile's time); a reduce kernel adds the pieces.
+// 4096^3: 1024 tiles = 6 x 152 + 112; 112 x 4 quarters = 2.95 rounds of
+// quarter tiles instead of one round of whole tiles.
+struct SplitTail {
+    int64_t full;   // tiles of the full rounds (one-tile grid)
+    int64_t rest;   // remainder tiles
+    int parts;
+};
+
+bool split_tail(const Problem& p, const Device& dev, SplitTail* st) {
     if (p.k < kShortK) return false;
     const int64_t G = dev.sm_count;
     const int64_t tiles = static_cast<int64_t>((p.m + 127) / 128) * ((p.n + kBN - 1) / kBN);
     const int64_t KT = (p.k + kBK - 1) / kBK;
-    const int64_t waves = (tiles + G - 1) / G;
-    return sk_has_region(tiles, KT, G) && 10 * tiles < 9 * waves * G;
+    const int64_t r = tiles % G;
+    if (r == 0 || 10 * r >= 9 * G) return false;
+    double best = 0.95;   // a round of whole tiles costs 1; require a 5 % gain
+    int parts = 1;
+    for (int s = 2; s <= 8 && KT / s >= 2 * kStages; ++s) {
+        const double t = static_cast<double>((r * s + G - 1) / G) / s;
+        if (t < best) {
+            best = t;
+            parts = s;
+        }
+    }
+    if (parts == 1) return false;
+    *st = SplitTail{tiles - r, r, parts};
+    return true;
+}
+
+bool make_maps(const Problem& p, CUtensorMap* ta, CUtensorMap* tb) {
+    using F = FCfg<4>;
+    return make_tensor_map(ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.A, p.m, p.k, p.lda, F::BM, kBK,
+                           kBK == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_tensor_map(tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.k, p.n, p.ldb, kBK, kBN,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+cudaError_t launch_split_tail(const Problem& p, const Device& dev, void* workspace, const SplitTail& st) {
+    using F = FCfg<4>;
+    if (!workspace) {
+        set_error("ffma_f32: split remainder launched without its workspace");
+        return cudaErrorInvalidValue;
+    }
+    CUtensorMap ta, tb;
+    if (!make_maps(p, &ta, &tb)) return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(ffma_f32_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(F::SMEM));
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(ffma_f32_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(F::SMEM));
+    if (err != cudaSuccess) {
+        set_error("cudaFuncSetAttribute(ffma_f32 kernels): %s", cudaGetErrorString(err));
+        return err;
+    }
+    const int vec_store = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
+    float* ws = static_cast<float*>(workspace);
+    if (st.full > 0) {
+        ffma_f32_kernel<4><<<static_cast<unsigned>(st.full), F::THREADS, F::SMEM, p.stream>>>(
+            ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status);
+        count_launch();
+    }
+    ffma_f32_split_kernel<<<static_cast<unsigned>(st.rest * st.parts), F::THREADS, F::SMEM, p.stream>>>(
+        ta, tb, ws, p.m, p.n, p.k, static_cast<int>(st.full), st.parts, dev.status);
+    count_launch();
+    ffma_f32_reduce_kernel<<<static_cast<unsigned>(st.rest), F::THREADS, 0, p.stream>>>(
+        ws, p.C, p.ldc, p.m, p.n, static_cast<int>(st.full), st.parts, vec_store);
+    count_launch();
+    err = cudaGetLastError();
+    if (err != cudaSuccess) set_error("ffma_f32 split launches: %s", cudaGetErrorString(err));
+    return err;
 }
 
 }  // namespace
 
 uint64_t ffma_f32_workspace_bytes(const Problem& p, const Device& dev) {
-    if (!use_stream_k(p, dev)) return 0;
-    return static_cast<uint64_t>(dev.sm_count) * (FCfg<4>::BM * kBN * sizeof(float) + sizeof(unsigned));
+    SplitTail st;
+    if (!split_tail(p, dev, &st)) return 0;
+    return static_cast<uint64_t>(st.rest) * st.parts * FCfg<4>::BM * kBN * sizeof(float);
 }
 
 cudaError_t launch_ffma_f32(const Problem& p, const Device& dev, void* workspace) {
-    if (p.k < kShortK) return launch_wr<2>(p, dev, nullptr);
-    if (use_stream_k(p, dev)) {
-        if (!workspace) {
-            set_error("ffma_f32: stream-K form launched without its workspace");
-            return cudaErrorInvalidValue;
-        }
-        return launch_wr<4>(p, dev, workspace);
-    }
-    return launch_wr<4>(p, dev, nullptr);
+    if (p.k < kShortK) return launch_wr<2>(p, dev);
+    SplitTail st;
+    if (split_tail(p, dev, &st)) return launch_split_tail(p, dev, workspace, st);
+    return launch_wr<4>(p, dev);
 }
 
 }  // namespace tgemm

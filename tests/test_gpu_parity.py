@@ -69,17 +69,17 @@ def test_irregular_4097x3001x1023(mode):
     parity.full_check(mode, inputs.make("irregular"))
 
 
-# The fp32 kernel's persistent form (k >= 2048, and a one-tile-per-CTA grid
-# would leave at least a tenth of its slots empty): rounds of whole tiles,
-# then a stream-K region where tiles are split between two CTAs and the CTA
-# holding a tile's first k-phases adds the other's partial sums.  One round,
-# one round, no round, three rounds before the stream-K region; ragged in m,
-# n and k, checked over the whole output.
-STREAM_K_SHAPES = [(2432, 2100, 2050), (2500, 2000, 2300), (2000, 2000, 4100), (500, 20000, 2050)]
+# The fp32 split remainder (k >= 2048 and a partly empty last wave): the
+# one-tile grid covers the full rounds, the tiles left are cut along k into
+# pieces whose partial sums a reduce kernel adds in part order.  Full rounds
+# then 19 tiles in 8 pieces; no full round (64 tiles in 7 pieces); 4 rounds
+# then 20 tiles in 7; 1 round then 104 tiles in 7.  Ragged in m, n and k,
+# checked over the whole output.
+SPLIT_SHAPES = [(2432, 2100, 2050), (1000, 900, 4100), (500, 20000, 2050), (2000, 2000, 4100)]
 
 
-@pytest.mark.parametrize("shape", STREAM_K_SHAPES, ids=lambda s: "x".join(map(str, s)))
-def test_fp32_persistent_schedule(shape):
+@pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_fp32_split_remainder(shape):
     m, n, k = shape
     parity.full_check("f32", inputs.random_case(7000 + m + n + k, m, n, k, kind="int"), f"f32 int {shape}")
     case = inputs.random_case(8000 + m + n + k, m, n, k, kind="uniform")

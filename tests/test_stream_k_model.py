@@ -1,22 +1,26 @@
-"""The fp32 kernel's persistent schedule, restated from csrc/ffma_f32.cu and checked on the CPU.
+"""Schedules that fill the last wave, restated from the sources and checked on the CPU.
 
 The pages' tiled algorithm (hecess.blogspot.com "[Multi-Core & GPU
 Programming] CUDA - Matrix Multiplication", "Tiled Matrix Multiplication
 Kernel") gives every output tile to one block, which walks all of its k
-phases.  With 1024 tiles of 128 x 128 on 152 SMs that leaves a last wave of
-112 tiles (0.74 of a wave).  The persistent form runs one CTA per SM: with
-T = q G + r tiles on G CTAs, CTA b first takes whole tiles b, b + G, ... for
-q - 1 rounds (G consecutive tiles in flight, as in the one-tile-per-block
-grid), then the last G + r tiles are flattened into (tile, k-phase)
-iterations and cut into G equal runs ("stream-K").  A tile whose phases fall
-to two CTAs is finished by the one holding its first phases (the head), which
-adds the other's partial sums (the tail) after waiting for its flag.  With
-r = 0, or r KT < G, there is no stream-K region.
+phases.  With T tiles on G = 152 SMs the last wave is partly empty (4096^3
+fp32: 1024 tiles = 6 x 152 + 112).
 
-Checked here: every iteration done once, every C tile stored once, at most one
+* csrc/ffma_f32.cu (split remainder): the one-tile grid runs the 6 full
+  rounds; the 112 tiles left are cut along k into `parts` pieces chosen to
+  fill whole rounds best, each piece writes a partial tile to its workspace
+  slot, and a reduce kernel adds a tile's pieces in part order.
+* csrc/stream_k.cuh (tensor-core kernels): rounds of whole tiles b, b + G,
+  ..., then the last G + r tiles flattened into (tile, k-phase) iterations
+  cut into G equal runs; a tile split between two CTAs is finished by the one
+  holding its first phases (head), which adds the other's partial (tail)
+  after waiting for its flag.
+
+Checked here: every iteration done once, every tile stored once, at most one
 tail and one head per CTA, workspace slots in range, waits that cannot form a
 cycle (co-residency comes from the cooperative launch), consecutive tiles in
-each round, and, with exact integer data, head + tail equals the tile's sum.
+each round, and, with exact integer data, that the partial sums add up to the
+tile's sum.
 """
 import numpy as np
 import pytest
@@ -24,14 +28,63 @@ import pytest
 BM, BN, BK = 128, 128, 16
 
 
-def selected(m, n, k, sm_count, short_k=2048):
-    """The launcher's rule: long k, and the one-tile-per-block grid would leave
-    at least a tenth of its block slots empty, and there is a stream-K region."""
+def split_tail(m, n, k, G=152, short_k=2048, stages=4):
+    """(full-round tiles, remainder tiles, parts) of the fp32 launcher, or None."""
     tiles = -(-m // BM) * -(-n // BN)
     kt = -(-k // BK)
-    rounds, r = divmod(tiles, sm_count)
-    waves = -(-tiles // sm_count)
-    return k >= short_k and rounds >= 1 and r > 0 and r * kt >= sm_count and 10 * tiles < 9 * waves * sm_count
+    r = tiles % G
+    if k < short_k or r == 0 or 10 * r >= 9 * G:
+        return None
+    best, parts = 0.95, 1
+    for s in range(2, 9):
+        if kt // s < 2 * stages:
+            break
+        t = -(-(r * s) // G) / s
+        if t < best:
+            best, parts = t, s
+    return None if parts == 1 else (tiles - r, r, parts)
+
+
+def test_split_tail_choices():
+    assert split_tail(4096, 4096, 4096) == (912, 112, 4)      # 112 x 4 quarters = 2.95 rounds
+    assert split_tail(1024, 1024, 4096) == (0, 64, 7)          # less than one wave: all split
+    assert split_tail(8192, 8192, 2048) is None                # 4096 tiles: last round 95 % full
+    assert split_tail(4096, 4096, 1024) is None                # short k: 64-row one-tile form
+    for shape in [(2432, 2100, 2050), (1000, 900, 4100), (500, 20000, 2050), (2000, 2000, 4100)]:
+        assert split_tail(*shape) is not None
+
+
+@pytest.mark.parametrize("shape", [(4096, 4096, 4096), (2432, 2100, 2050), (1000, 900, 4100),
+                                   (500, 20000, 2050), (3000, 6000, 4096)])
+def test_split_tail_covers_every_phase_once(shape):
+    m, n, k = shape
+    full, rest, parts = split_tail(m, n, k)
+    kt = -(-k // BK)
+    tiles = full + rest
+    done = np.zeros((tiles, kt), dtype=np.int64)
+    done[:full] += 1                                           # one-tile grid: blocks 0 .. full-1
+    for u in range(rest * parts):                              # split kernel: block u -> slot u
+        t, part = full + u // parts, u % parts
+        k0, k1 = kt * part // parts, kt * (part + 1) // parts
+        assert k1 - k0 >= 7
+        done[t, k0:k1] += 1
+    assert (done == 1).all()
+    # reduce block b reads slots b * parts .. b * parts + parts - 1, all written
+    assert {b * parts + q for b in range(rest) for q in range(parts)} == set(range(rest * parts))
+
+
+def test_split_tail_sums_exactly_on_integers():
+    rng = np.random.default_rng(3)
+    k, parts = 160, 3
+    kt = k // BK
+    A = rng.integers(-8, 9, size=(BM, k)).astype(np.float32)
+    B = rng.integers(-8, 9, size=(k, BN)).astype(np.float32)
+    slots = [A[:, kt * q // parts * BK:kt * (q + 1) // parts * BK] @ B[kt * q // parts * BK:kt * (q + 1) // parts * BK]
+             for q in range(parts)]
+    C = np.zeros((BM, BN), dtype=np.float32)
+    for q in range(parts):                                     # part order, as the reduce kernel
+        C += slots[q]
+    np.testing.assert_array_equal(C, A @ B)
 
 
 def plan(tiles, kt, b, grid):
@@ -45,10 +98,8 @@ def plan(tiles, kt, b, grid):
     return n_dp, tiles - tiles_sk, total * b // grid, total * (b + 1) // grid
 
 
-def segments(m, n, k, grid):
+def segments_of(tiles, kt, grid):
     """Per CTA, its segments (tile, first k-phase, end k-phase), in its own order."""
-    tiles = -(-m // BM) * -(-n // BN)
-    kt = -(-k // BK)
     out = []
     for b in range(grid):
         n_dp, t_sk0, v, v1 = plan(tiles, kt, b, grid)
@@ -59,7 +110,7 @@ def segments(m, n, k, grid):
             segs.append((t_sk0 + q, ka, kz))
             v += kz - ka
         out.append(segs)
-    return out, tiles, kt
+    return out
 
 
 def roles(segs, kt):
@@ -75,15 +126,15 @@ def roles(segs, kt):
     return r
 
 
-SHAPES = [(4096, 4096, 4096), (4097, 3001, 2048), (8192, 8192, 2048), (3000, 6000, 4096),
-          (4096, 4096, 8192), (2432, 1000, 2100), (2100, 1100, 2048), (2000, 2000, 4096)]
+# (tiles, KT) of persistent tensor-core launches: 256 x 256 tiles (KT for
+# 128 bytes of k per phase) and some that leave a partial last wave.
+PLANS = [(256, 128), (1024, 128), (156, 49), (176, 16), (198, 65), (628, 129), (304, 64), (153, 128)]
 
 
 @pytest.mark.parametrize("sm_count", [152, 148, 132])
-@pytest.mark.parametrize("shape", SHAPES)
-def test_schedule_invariants(shape, sm_count):
-    m, n, k = shape
-    per_cta, tiles, kt = segments(m, n, k, sm_count)
+@pytest.mark.parametrize("tiles,kt", PLANS)
+def test_schedule_invariants(tiles, kt, sm_count):
+    per_cta = segments_of(tiles, kt, sm_count)
     done = np.zeros((tiles, kt), dtype=np.int64)
     stores = np.zeros(tiles, dtype=np.int64)
     for b, segs in enumerate(per_cta):
@@ -108,30 +159,15 @@ def test_schedule_invariants(shape, sm_count):
     # Round j of whole tiles: the CTAs hold G consecutive tiles (L2 reuse as in the plain grid).
     n_dp0 = plan(tiles, kt, 0, sm_count)[0]
     for j in range(n_dp0):
-        held = sorted(per_cta[b][j][0] for b in range(sm_count) if len(per_cta[b]) > j
-                      and roles(per_cta[b], kt)[j] == "store" and j < plan(tiles, kt, b, sm_count)[0])
+        held = sorted(per_cta[b][j][0] for b in range(sm_count) if j < plan(tiles, kt, b, sm_count)[0])
         assert held == list(range(held[0], held[0] + len(held)))
 
 
-def test_selection_and_regions():
+def test_plan_regions():
     G = 152
-    assert plan(1024, 256, 0, G)[:2] == (5, 1024 - 264)       # 4096^3: 5 rounds, then 264 tiles stream-K
-    assert not selected(4096, 4096, 4096, G)                  # ... but 6.7 waves fill 96 % of the slots
-    assert not selected(3000, 6000, 4096, G)                  # 7.4 waves: 93 %
-    assert selected(2500, 2000, 2300, G)                      # 2.1 waves: 70 %
-    assert not selected(1024, 1024, 4096, G)                  # 64 tiles: less than one wave
-    assert not selected(4096, 4096, 1024, G)                  # short k: 64-row one-tile-per-block form
+    assert plan(1024, 256, 0, G)[:2] == (5, 1024 - 264)       # 5 rounds, then 264 tiles stream-K
     assert plan(152, 132, 7, G) == (1, 152, 0, 0)             # r = 0: whole tiles only
     assert plan(153, 128, 0, G)[:2] == (2, 153) and plan(153, 128, 1, G)[0] == 1   # r KT < G
-    assert not selected(2432, 1000, 2100, G) and not selected(2100, 1100, 2048, G)
-    # the ragged shapes the GPU parity tests run through the persistent kernel:
-    # one round then stream-K, no rounds, three rounds then stream-K
-    for shape, n_dp in [((2432, 2100, 2050), 1), ((2500, 2000, 2300), 1), ((2000, 2000, 4100), 0),
-                        ((500, 20000, 2050), 3)]:
-        assert selected(*shape, G)
-        per_cta, tiles, kt = segments(*shape, G)
-        assert plan(tiles, kt, 0, G)[0] == n_dp
-        assert sum(roles(s, kt).count("head") for s in per_cta) > 100
 
 
 def test_head_plus_tail_is_the_full_sum_on_integers():
@@ -141,7 +177,8 @@ def test_head_plus_tail_is_the_full_sum_on_integers():
     m, n, k, grid = 600, 260, 96, 4
     kt = k // BK
     tiles_m = -(-m // BM)
-    per_cta, tiles, _ = segments(m, n, k, grid)
+    tiles = tiles_m * -(-n // BN)
+    per_cta = segments_of(tiles, kt, grid)
     assert plan(tiles, kt, 0, grid)[:2] == (2, 8)
     assert sum(roles(s, kt).count("head") for s in per_cta) == grid - 1
     A = rng.integers(-8, 9, size=(m, k)).astype(np.float32)
@@ -200,15 +237,6 @@ def test_umma_stream_k_shapes(mode):
     for shape in [(3300, 3000, 3100), (2000, 2600, 1000), (2600, 4000, 4100)]:
         bn, tiles, kt, sk = umma_choice(*shape, mode)
         assert sk, shape
-        per_cta = []
-        for b in range(G):
-            n_dp, t_sk0, v, v1 = plan(tiles, kt, b, G)
-            segs = [(b + j * G, 0, kt) for j in range(n_dp)]
-            while v < v1:
-                q, ka = divmod(v, kt)
-                kz = min(kt, ka + (v1 - v))
-                segs.append((t_sk0 + q, ka, kz))
-                v += kz - ka
-            per_cta.append(segs)
+        per_cta = segments_of(tiles, kt, G)
         assert sum(roles(s, kt).count("head") for s in per_cta) > 20
     assert not umma_choice(1024, 1024, 1024, mode)[3]   # fewer tiles than SMs
