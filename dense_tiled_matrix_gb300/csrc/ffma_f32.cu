@@ -253,13 +253,14 @@ ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 // -- with the data-parallel kernel's pipeline and stores its partial sums in
 // slot u of `ws` (float4 j of thread t at j * THREADS + t, so a warp stores
 // 512 contiguous bytes).
-__global__ void __launch_bounds__(FCfg<4>::THREADS, 1)
+template <int WR>
+__global__ void __launch_bounds__(FCfg<WR>::THREADS, FCfg<WR>::MIN_BLOCKS)
 ffma_f32_split_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       float* __restrict__ ws, int M, int N, int K, int tile0, int parts, uint32_t* status) {
-    using F = FCfg<4>;
+    using F = FCfg<WR>;
     constexpr int kBM = F::BM;
     extern __shared__ uint8_t smem_raw[];
-    const Smem<4> sm(smem_raw);
+    const Smem<WR> sm(smem_raw);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -330,10 +331,11 @@ ffma_f32_split_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
 
 // C of the remainder tiles: tile tile0 + b is the sum of the split kernel's
 // slots b * parts .. b * parts + parts - 1, added in part order.
-__global__ void __launch_bounds__(FCfg<4>::THREADS)
+template <int WR>
+__global__ void __launch_bounds__(FCfg<WR>::THREADS)
 ffma_f32_reduce_kernel(const float* __restrict__ ws, float* __restrict__ C, int64_t ldc, int M, int N, int tile0,
                        int parts, int vec_store) {
-    using F = FCfg<4>;
+    using F = FCfg<WR>;
     constexpr int kBM = F::BM;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wm = warp >> 1, wn = warp & 1;
@@ -391,22 +393,24 @@ cudaError_t launch_wr(const Problem& p, const Device& dev) {
 // 64-row CTAs per SM; 4097 x 3001 x 1024 42.8 vs 46.3.
 constexpr int kShortK = 2048;
 
-// Split remainder: the one-tile grid runs the q G tiles of the full rounds;
-// the r tiles left (r < 0.9 G) are cut along k into `parts` pieces, chosen
-// so that r * parts pieces fill whole rounds of the grid best (each round of
-// pieces takes 1/parts of a tile's time); a reduce kernel adds the pieces.
-// 4096^3: 1024 tiles = 6 x 152 + 112; 112 x 4 quarters = 2.95 rounds of
-// quarter tiles instead of one round of whole tiles.
+// Split remainder: the one-tile grid runs the tiles of its full rounds (G
+// slots a round: SMs x resident CTAs per SM); the r tiles left (r < 0.9 G)
+// are cut along k into `parts` pieces, chosen so that r * parts pieces fill
+// whole rounds best (each round of pieces takes 1/parts of a tile's time); a
+// reduce kernel adds the pieces.  4096^3 (128-row tiles, 152 slots): 1024 =
+// 6 x 152 + 112 tiles; 112 x 4 quarters = 2.95 rounds of quarter tiles
+// instead of one round of whole tiles.
 struct SplitTail {
     int64_t full;   // tiles of the full rounds (one-tile grid)
     int64_t rest;   // remainder tiles
     int parts;
 };
 
+template <int WR>
 bool split_tail(const Problem& p, const Device& dev, SplitTail* st) {
-    if (p.k < kShortK) return false;
-    const int64_t G = dev.sm_count;
-    const int64_t tiles = static_cast<int64_t>((p.m + 127) / 128) * ((p.n + kBN - 1) / kBN);
+    using F = FCfg<WR>;
+    const int64_t G = static_cast<int64_t>(dev.sm_count) * F::MIN_BLOCKS;
+    const int64_t tiles = static_cast<int64_t>((p.m + F::BM - 1) / F::BM) * ((p.n + kBN - 1) / kBN);
     const int64_t KT = (p.k + kBK - 1) / kBK;
     const int64_t r = tiles % G;
     if (r == 0 || 10 * r >= 9 * G) return false;
@@ -424,26 +428,23 @@ bool split_tail(const Problem& p, const Device& dev, SplitTail* st) {
     return true;
 }
 
-bool make_maps(const Problem& p, CUtensorMap* ta, CUtensorMap* tb) {
-    using F = FCfg<4>;
-    return make_tensor_map(ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.A, p.m, p.k, p.lda, F::BM, kBK,
-                           kBK == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) &&
-           make_tensor_map(tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.k, p.n, p.ldb, kBK, kBN,
-                           CU_TENSOR_MAP_SWIZZLE_NONE);
-}
-
+template <int WR>
 cudaError_t launch_split_tail(const Problem& p, const Device& dev, void* workspace, const SplitTail& st) {
-    using F = FCfg<4>;
+    using F = FCfg<WR>;
     if (!workspace) {
         set_error("ffma_f32: split remainder launched without its workspace");
         return cudaErrorInvalidValue;
     }
     CUtensorMap ta, tb;
-    if (!make_maps(p, &ta, &tb)) return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(ffma_f32_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (!make_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.A, p.m, p.k, p.lda, F::BM, kBK,
+                         kBK == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.k, p.n, p.ldb, kBK, kBN,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(ffma_f32_kernel<WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(F::SMEM));
     if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(ffma_f32_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(ffma_f32_split_kernel<WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(F::SMEM));
     if (err != cudaSuccess) {
         set_error("cudaFuncSetAttribute(ffma_f32 kernels): %s", cudaGetErrorString(err));
@@ -452,14 +453,14 @@ cudaError_t launch_split_tail(const Problem& p, const Device& dev, void* workspa
     const int vec_store = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
     float* ws = static_cast<float*>(workspace);
     if (st.full > 0) {
-        ffma_f32_kernel<4><<<static_cast<unsigned>(st.full), F::THREADS, F::SMEM, p.stream>>>(
+        ffma_f32_kernel<WR><<<static_cast<unsigned>(st.full), F::THREADS, F::SMEM, p.stream>>>(
             ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status);
         count_launch();
     }
-    ffma_f32_split_kernel<<<static_cast<unsigned>(st.rest * st.parts), F::THREADS, F::SMEM, p.stream>>>(
+    ffma_f32_split_kernel<WR><<<static_cast<unsigned>(st.rest * st.parts), F::THREADS, F::SMEM, p.stream>>>(
         ta, tb, ws, p.m, p.n, p.k, static_cast<int>(st.full), st.parts, dev.status);
     count_launch();
-    ffma_f32_reduce_kernel<<<static_cast<unsigned>(st.rest), F::THREADS, 0, p.stream>>>(
+    ffma_f32_reduce_kernel<WR><<<static_cast<unsigned>(st.rest), F::THREADS, 0, p.stream>>>(
         ws, p.C, p.ldc, p.m, p.n, static_cast<int>(st.full), st.parts, vec_store);
     count_launch();
     err = cudaGetLastError();
@@ -471,15 +472,15 @@ cudaError_t launch_split_tail(const Problem& p, const Device& dev, void* workspa
 
 uint64_t ffma_f32_workspace_bytes(const Problem& p, const Device& dev) {
     SplitTail st;
-    if (!split_tail(p, dev, &st)) return 0;
-    return static_cast<uint64_t>(st.rest) * st.parts * FCfg<4>::BM * kBN * sizeof(float);
+    if (p.k < kShortK)
+        return split_tail<2>(p, dev, &st) ? static_cast<uint64_t>(st.rest) * st.parts * FCfg<2>::BM * kBN * 4 : 0;
+    return split_tail<4>(p, dev, &st) ? static_cast<uint64_t>(st.rest) * st.parts * FCfg<4>::BM * kBN * 4 : 0;
 }
 
 cudaError_t launch_ffma_f32(const Problem& p, const Device& dev, void* workspace) {
-    if (p.k < kShortK) return launch_wr<2>(p, dev);
     SplitTail st;
-    if (split_tail(p, dev, &st)) return launch_split_tail(p, dev, workspace, st);
-    return launch_wr<4>(p, dev);
+    if (p.k < kShortK) return split_tail<2>(p, dev, &st) ? launch_split_tail<2>(p, dev, workspace, st) : launch_wr<2>(p, dev);
+    return split_tail<4>(p, dev, &st) ? launch_split_tail<4>(p, dev, workspace, st) : launch_wr<4>(p, dev);
 }
 
 }  // namespace tgemm
