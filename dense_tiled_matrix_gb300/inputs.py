@@ -123,6 +123,19 @@ def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return rounded.astype(np.uint16)
 
 
+def to_tf32(x: np.ndarray, mode: str = "rne") -> np.ndarray:
+    """fp32 values reduced to TF32 precision (10 stored mantissa bits), still as
+    float32: the low 13 mantissa bits cleared ("trunc") or rounded to nearest,
+    ties to even ("rne").  Finite inputs only."""
+    bits = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    if mode == "rne":
+        bits = bits + np.uint64(0xFFF) + ((bits >> np.uint64(13)) & np.uint64(1))
+    elif mode != "trunc":
+        raise ValueError(mode)
+    bits = bits & np.uint64(0xFFFFE000)
+    return bits.astype(np.uint32).view(np.float32)
+
+
 def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     """Exact fp32 values of bf16 bit patterns."""
     return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)

@@ -148,6 +148,27 @@ def test_repeat_runs_are_bit_identical(mode):
     assert torch.equal(c1, c2)
 
 
+def test_tf32_input_conversion(capsys):
+    """How the tensor core reduces fp32 operands to TF32 (the pages are silent):
+    the product agrees with the oracle on inputs reduced one way to within fp32
+    accumulation error, and with the other only to TF32 precision."""
+    m, n, k = 256, 256, 1024
+    case = inputs.random_case(4343, m, n, k, kind="uniform")
+    C = parity.run("tf32", case.A, case.B).cpu().numpy().astype(np.float64)
+    errs = {}
+    for conv in ("trunc", "rne"):
+        P, D = oracle.gemm(inputs.to_tf32(case.A, conv), inputs.to_tf32(case.B, conv))
+        errs[conv] = float(np.max(np.abs(C - P) / D))
+    best = min(errs, key=errs.get)
+    other = "rne" if best == "trunc" else "trunc"
+    with capsys.disabled():
+        print(f"\nTF32 operand conversion: {best} (max error {errs[best]:.2e}; {other}: {errs[other]:.2e})")
+    assert errs[best] <= 1e-5, errs
+    assert errs[other] > 10 * errs[best], errs
+    # Measured on GB300: truncation (5.8e-7 against the truncated-input oracle, 1.35e-4 against RNE).
+    assert best == "trunc", errs
+
+
 def _sampled_check(mode, case, n_rows, n_entries, seed):
     A_np, B_np = parity.inputs_for(mode, case)
     C = parity.run(mode, A_np, B_np)

@@ -74,3 +74,20 @@ def test_named_workloads_small():
     assert set(np.unique(I.make("int64").A).tolist()) <= set(range(-3, 4))
     cb = I.make("u128", "bf16")
     assert cb.A.dtype == np.uint16 and cb.dtype == "bf16"
+
+
+def test_tf32_reduction():
+    one = 1.0
+    ulp = 2.0 ** -10                      # TF32 spacing at 1
+    vals = np.array([one + ulp / 2,       # exact tie: even neighbour is 1
+                     one + ulp + ulp / 2, # tie: rounds up to 1 + 2 ulp (even)
+                     one + ulp / 2 + 2.0 ** -20,   # above the tie
+                     -(one + 3 * ulp / 4),
+                     3.0, 2.0 ** -100], dtype=np.float32)
+    rne = I.to_tf32(vals, "rne")
+    trunc = I.to_tf32(vals, "trunc")
+    assert rne.tolist() == [1.0, one + 2 * ulp, one + ulp, -(one + ulp), 3.0, 2.0 ** -100]
+    assert trunc.tolist() == [1.0, one + ulp, 1.0, -1.0, 3.0, 2.0 ** -100]
+    # 10 stored mantissa bits: the low 13 bits of every result are zero
+    r = I.to_tf32(I.uniform_pm1(5, 0, (1000,)), "rne")
+    assert not (r.view(np.uint32) & 0x1FFF).any()
