@@ -106,6 +106,19 @@ def test_tensor_core_split_tiles(mode, shape):
     assert torch.equal(parity.ENTRY[mode](A, B), parity.ENTRY[mode](A, B))
 
 
+# Extremes of k: 4096 k-phases on 4 tiles (the fp32 path splits them 8 ways,
+# 512 phases per piece; integer sums reach 2^20, still exact in fp32), and a
+# single k-phase over a large ragged output.
+EXTREME_K_SHAPES = [(256, 256, 65536), (4100, 8200, 16)]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", EXTREME_K_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_extreme_k(mode, shape):
+    m, n, k = shape
+    parity.full_check(mode, inputs.random_case(9900 + m + n + k, m, n, k, kind="int"), f"{mode} int {shape}")
+
+
 @pytest.mark.parametrize("mode", MODES)
 def test_leading_dimensions_and_untouched_padding(mode):
     m, n, k = 200, 150, 90

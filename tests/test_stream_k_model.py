@@ -54,6 +54,7 @@ def test_split_tail_choices():
     assert split_tail(4097, 3001, 1023) == (1520, 40, 7)       # 64-row tiles, 304 slots a round
     assert split_tail(8192, 8192, 512) is None                 # 8192 64-row tiles: no remainder
     assert split_tail(200, 150, 90) is None                    # 6 k-phases: too short to cut
+    assert split_tail(256, 256, 65536) == (0, 4, 8)            # 4 tiles, 4096 phases: 8 pieces each
     for shape in [(2432, 2100, 2050), (1000, 900, 4100), (500, 20000, 2050), (2000, 2000, 4100)]:
         assert split_tail(*shape) is not None
 
