@@ -182,6 +182,32 @@ def test_tf32_input_conversion(capsys):
     assert best == "trunc", errs
 
 
+def _boundary_shapes(count, seed, budget=1.2e9):
+    """Seeded shapes that sit near the dispatch boundaries: m around 64 (the
+    skinny bf16 kernel), sizes around multiples of 64/128/224/256 (tile edges),
+    k around 2048 and 3072 (fp32 tile height, tensor-core tile height) and
+    tile counts around multiples of 152 (a partly empty last wave: split
+    pieces, 224-wide tiles, stream-K)."""
+    rng = np.random.default_rng(seed)
+    near = lambda base: int(max(1, base + rng.integers(-3, 4)))
+    out = []
+    while len(out) < count:
+        m = near(int(rng.choice([1, 16, 32, 48, 64, 65, 128, 256, 1024, 1536, 2048, 2432, 3072])))
+        n = near(int(rng.choice([8, 64, 128, 224, 256, 448, 896, 1536, 2048, 2432, 3072])))
+        k = near(int(rng.choice([1, 16, 64, 129, 1024, 2048, 2049, 3072, 3100])))
+        if m * n * k <= budget:
+            out.append((m, n, k))
+    return out
+
+
+@pytest.mark.parametrize("shape", _boundary_shapes(36, 2024), ids=lambda s: "x".join(map(str, s)))
+def test_boundary_shapes_exact(shape):
+    m, n, k = shape
+    case = inputs.random_case(31 * m + 7 * n + k, m, n, k, kind="int")
+    for mode in MODES:
+        parity.full_check(mode, case, f"{mode} int {shape}")
+
+
 def _sampled_check(mode, case, n_rows, n_entries, seed):
     A_np, B_np = parity.inputs_for(mode, case)
     C = parity.run(mode, A_np, B_np)
