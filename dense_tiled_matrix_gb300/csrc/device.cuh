@@ -122,6 +122,15 @@ __device__ __forceinline__ void bulk_wait_group() {
     asm volatile("cp.async.bulk.wait_group %0;" :: "n"(N) : "memory");
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialisation may start while the kernel before it in the stream is still
+// running; griddep_wait() returns once that kernel has completed and its
+// memory operations are visible, so everything before it must not touch
+// global memory the previous kernel writes.  griddep_launch_dependents()
+// lets the next such kernel be launched before this one finishes.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Orders this thread's ordinary shared-memory accesses before later accesses
 // by the async proxy (TMA) and vice versa.
 __device__ __forceinline__ void fence_proxy_async_smem() {

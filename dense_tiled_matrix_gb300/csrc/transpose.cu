@@ -71,6 +71,7 @@ transpose_tma_kernel(const __grid_constant__ CUtensorMap tm_src, const __grid_co
     float* out = reinterpret_cast<float*>(base + kXStages * kXTileBytes);   // 2 x [kXC][kXR]
     uint64_t* full = reinterpret_cast<uint64_t*>(base + (kXStages + 2) * kXTileBytes);
 
+    griddep_launch_dependents();   // the product that reads dst may be launched now; it waits for us
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int tiles_c = (cols + kXC - 1) / kXC;
     const int64_t tiles = static_cast<int64_t>((rows + kXR - 1) / kXR) * tiles_c;

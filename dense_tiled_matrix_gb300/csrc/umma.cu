@@ -73,6 +73,7 @@ struct Cfg {
 };
 
 constexpr int kThreads = 192;
+constexpr bool kPdl = true;   // whole-tile launches may start behind the previous kernel
 
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group_m, int& tm,
                                             int& tn) {
@@ -159,6 +160,9 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Launched right behind the previous kernel in the stream (e.g. the B
+    // transpose of the TF32 path): wait for it before any global access.
+    griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
@@ -392,6 +396,14 @@ cudaError_t launch(const Problem& p, const Device& dev, void* workspace) {
     cfg.dynamicSmemBytes = G::SMEM;
     cfg.stream = p.stream;
     cfg.gridDim = dim3(static_cast<unsigned>(tiles < dev.sm_count ? tiles : dev.sm_count), 1, 1);
+    if (!kSK && kPdl) {
+        // The prologue (barriers, tensor memory) overlaps the previous kernel's
+        // tail; the kernel waits for it before touching global memory.
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
     if (kSK) {
         if (!workspace) {
             set_error("umma_kernel: stream-K form launched without its workspace");
