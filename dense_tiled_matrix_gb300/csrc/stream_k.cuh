@@ -1,6 +1,6 @@
-// stream_k.cuh -- the persistent schedule shared by the fp32 FFMA kernel and
-// the tcgen05 kernels: whole-tile rounds, then a stream-K region whose tiles
-// may be split along k between two CTAs, and the flag hand-over between them.
+// stream_k.cuh -- the persistent schedule of the tcgen05 kernels' stream-K
+// form: whole-tile rounds, then a stream-K region whose tiles may be split
+// along k between two CTAs, and the flag hand-over between them.
 #pragma once
 
 #include <cstdint>
