@@ -31,6 +31,10 @@
 //    tile rows; the epilogue writes 4 rows x 128 contiguous bytes per warp
 //    instruction with 128-bit stores.
 //
+//  * Roles.  The 128-row kernel is warp-specialised: one warp group only
+//    streams tiles with TMA, two multiply, and the register file is re-split
+//    between them (setmaxnreg); the 64-row kernel used for short k keeps the
+//    producer in thread 0 of its consumers.
 //  * The last wave.  With T = q G + r tiles on G SMs (r < 0.9 G), the one-tile
 //    grid runs the q G tiles of the full rounds and the r tiles left are cut
 //    along k into `parts` pieces that fill whole rounds best; each piece's
@@ -171,6 +175,118 @@ struct Smem {
         empty = full + kStages;
     }
 };
+
+// 128-row tiles, warp-specialised.  Warp group 0 streams the operand tiles:
+// one thread issues the TMA copies of each k-phase as soon as its stage is
+// free; warp groups 1-2 (8 warps, the thread layout below) multiply.  The
+// register file is re-split once at the start -- the producer group keeps
+// 24 registers a thread, the consumer groups take 240 -- so the consumers
+// keep the 8 x 8 register tile while their loop carries no producer branch
+// (measured on GB300: 4096^3 54.0 -> 57.0 TFLOP/s; with the producer in lane
+// 0 of every warp in turn it fell to 51.2).  Block u computes, with
+// parts == 1, tile tile0 + u and stores it in C; with parts > 1, piece
+// u % parts (k-phases [KT p / parts, KT (p + 1) / parts)) of tile
+// tile0 + u / parts, whose partial sums go to slot u of `ws` (float4 j of
+// consumer thread t at j * 256 + t) for ffma_f32_reduce_kernel<4>.
+constexpr int kWsThreads = 384;
+constexpr int kProducerRegs = 24, kConsumerRegs = 240;
+static_assert(128 * kProducerRegs + 256 * kConsumerRegs <= 65536, "register split exceeds the file");
+
+__global__ void __launch_bounds__(kWsThreads, 1)
+ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   float* __restrict__ C, int64_t ldc, int M, int N, int K, int vec_store, uint32_t* status,
+                   int tile0, int parts, float* __restrict__ ws) {
+    using F = FCfg<4>;
+    constexpr int kBM = F::BM;
+    extern __shared__ uint8_t smem_raw[];
+    const Smem<4> sm(smem_raw);
+    const int warp_all = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    // Tile origin and k-range of this block (recomputed where needed rather
+    // than held in registers through the consumers' loop).
+    auto origin = [&](int& m0, int& n0) {
+        int tile_m, tile_n;
+        tile_coords(tile0 + (parts > 1 ? static_cast<int>(blockIdx.x) / parts : static_cast<int>(blockIdx.x)),
+                    (M + kBM - 1) / kBM, (N + kBN - 1) / kBN, tile_m, tile_n);
+        m0 = tile_m * kBM;
+        n0 = tile_n * kBN;
+    };
+    auto k_range = [&](int& k0, int& NI) {
+        const int KT = (K + kBK - 1) / kBK;
+        const int part = parts > 1 ? static_cast<int>(blockIdx.x) % parts : 0;
+        k0 = static_cast<int>(static_cast<int64_t>(KT) * part / parts);
+        NI = static_cast<int>(static_cast<int64_t>(KT) * (part + 1) / parts) - k0;
+    };
+    if (threadIdx.x == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sm.full[s], 1);
+            mbar_init(&sm.empty[s], F::WARPS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp_all < 4) {
+        // ---------------------------------------------------- producer --
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kProducerRegs));
+        if (threadIdx.x == 0) {
+            int m0, n0, k0, NI;
+            origin(m0, n0);
+            k_range(k0, NI);
+            for (int i = 0; i < NI; ++i) {
+                const int s = i % kStages;
+                if (i >= kStages && !mbar_wait(&sm.empty[s], static_cast<uint32_t>(i / kStages - 1) & 1u, status))
+                    break;   // the consumers time out on the stages never filled
+                mbar_arrive_expect_tx(&sm.full[s], F::STAGE_A + kStageB);
+                tma_load_2d(sm.sA + s * (kBM * kBK), &tmA, &sm.full[s], (k0 + i) * kBK, m0);
+                tma_load_2d(sm.sB + s * (kBK * kBN), &tmB, &sm.full[s], n0, (k0 + i) * kBK);
+            }
+        }
+        return;
+    }
+
+    // --------------------------------------------------------- consumers --
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kConsumerRegs));
+    const int ctid = threadIdx.x - 128;
+    const int warp = ctid >> 5;
+    // Thread layout: warp (wm, wn) covers rows 32*wm .. +31 and columns
+    // 64*wn .. +63; lane (tm, tn) takes rows tm + 4i (i < 8) and columns
+    // 4*tn .. +3 and 32 + 4*tn .. +3 of that warp tile.
+    const int wm = warp >> 1, wn = warp & 1;
+    const int tm = lane >> 3, tn = lane & 7;
+    const int a_row0 = 32 * wm + tm;
+    const int b_col0 = 64 * wn + 4 * tn;
+    // 64-byte swizzle: 16-byte chunk c of tile row r sits at chunk c ^ ((r >> 1) & 3).
+    // For r = a_row0 + 4i this is (tm >> 1) ^ (2 * (i & 1)).
+    const int swz_even = kBK == 16 ? (tm >> 1) : tm;
+    int k0, NI;
+    k_range(k0, NI);
+    Acc acc;
+    zero(acc);
+    int s = 0;
+    uint32_t phase = 0;
+    for (int i = 0; i < NI; ++i) {
+        if (!mbar_wait(&sm.full[s], phase, status)) return;   // status records the timeout
+        fma_phase(acc, sm.sA + s * (kBM * kBK), sm.sB + s * (kBK * kBN), a_row0, b_col0, swz_even);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[s]);
+        if (++s == kStages) { s = 0; phase ^= 1u; }
+    }
+    if (parts == 1) {
+        int m0, n0;
+        origin(m0, n0);
+        store_tile(acc, C, ldc, M, N, m0, n0, a_row0, b_col0, vec_store);
+        return;
+    }
+    float4* dst = reinterpret_cast<float4*>(ws + static_cast<int64_t>(blockIdx.x) * kBM * kBN) + ctid;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int p = 0; p < 4; p += 2)
+            dst[(i * 2 + p / 2) * F::THREADS] = make_float4(acc[i][p].x, acc[i][p].y, acc[i][p + 1].x, acc[i][p + 1].y);
+}
 
 // Data-parallel form: one CTA per C tile, which walks all of its k-phases.
 template <int WR>
@@ -363,6 +479,21 @@ ffma_f32_reduce_kernel(const float* __restrict__ ws, float* __restrict__ C, int6
     store_tile(acc, C, ldc, M, N, tile_m * kBM, tile_n * kBN, a_row0, b_col0, vec_store);
 }
 
+// The warp-specialised 128-row kernel over `grid` blocks (see its comment).
+cudaError_t launch_ws(const Problem& p, const CUtensorMap& ta, const CUtensorMap& tb, int64_t grid, int64_t tile0,
+                      int parts, float* ws, int vec_store, const Device& dev) {
+    cudaError_t err = cudaFuncSetAttribute(ffma_f32_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(FCfg<4>::SMEM));
+    if (err != cudaSuccess) {
+        set_error("cudaFuncSetAttribute(ffma_f32_ws_kernel): %s", cudaGetErrorString(err));
+        return err;
+    }
+    ffma_f32_ws_kernel<<<static_cast<unsigned>(grid), kWsThreads, FCfg<4>::SMEM, p.stream>>>(
+        ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status, static_cast<int>(tile0), parts, ws);
+    count_launch();
+    return cudaSuccess;
+}
+
 // Launches the one-tile-per-CTA kernel over all tiles.
 template <int WR>
 cudaError_t launch_wr(const Problem& p, const Device& dev) {
@@ -373,18 +504,23 @@ cudaError_t launch_wr(const Problem& p, const Device& dev) {
         !make_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.k, p.n, p.ldb, kBK, kBN,
                          CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(ffma_f32_kernel<WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(F::SMEM));
-    if (err != cudaSuccess) {
-        set_error("cudaFuncSetAttribute(ffma_f32_kernel): %s", cudaGetErrorString(err));
-        return err;
-    }
     const int64_t tiles = static_cast<int64_t>((p.m + F::BM - 1) / F::BM) * ((p.n + kBN - 1) / kBN);
     const int vec_store = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
-    ffma_f32_kernel<WR><<<static_cast<unsigned>(tiles), F::THREADS, F::SMEM, p.stream>>>(
-        ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status);
-    count_launch();
-    err = cudaGetLastError();
+    cudaError_t err;
+    if constexpr (WR == 4) {
+        err = launch_ws(p, ta, tb, tiles, 0, 1, nullptr, vec_store, dev);
+    } else {
+        err = cudaFuncSetAttribute(ffma_f32_kernel<WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(F::SMEM));
+        if (err != cudaSuccess) {
+            set_error("cudaFuncSetAttribute(ffma_f32_kernel): %s", cudaGetErrorString(err));
+            return err;
+        }
+        ffma_f32_kernel<WR><<<static_cast<unsigned>(tiles), F::THREADS, F::SMEM, p.stream>>>(
+            ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status);
+        count_launch();
+    }
+    if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) set_error("ffma_f32_kernel launch: %s", cudaGetErrorString(err));
     return err;
 }
@@ -441,25 +577,32 @@ cudaError_t launch_split_tail(const Problem& p, const Device& dev, void* workspa
         !make_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.k, p.n, p.ldb, kBK, kBN,
                          CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(ffma_f32_kernel<WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(F::SMEM));
-    if (err == cudaSuccess)
-        err = cudaFuncSetAttribute(ffma_f32_split_kernel<WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(F::SMEM));
-    if (err != cudaSuccess) {
-        set_error("cudaFuncSetAttribute(ffma_f32 kernels): %s", cudaGetErrorString(err));
-        return err;
-    }
     const int vec_store = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
     float* ws = static_cast<float*>(workspace);
-    if (st.full > 0) {
-        ffma_f32_kernel<WR><<<static_cast<unsigned>(st.full), F::THREADS, F::SMEM, p.stream>>>(
-            ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status);
+    cudaError_t err = cudaSuccess;
+    if constexpr (WR == 4) {
+        if (st.full > 0) err = launch_ws(p, ta, tb, st.full, 0, 1, nullptr, vec_store, dev);
+        if (err == cudaSuccess) err = launch_ws(p, ta, tb, st.rest * st.parts, st.full, st.parts, ws, vec_store, dev);
+        if (err != cudaSuccess) return err;
+    } else {
+        err = cudaFuncSetAttribute(ffma_f32_kernel<WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(F::SMEM));
+        if (err == cudaSuccess)
+            err = cudaFuncSetAttribute(ffma_f32_split_kernel<WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(F::SMEM));
+        if (err != cudaSuccess) {
+            set_error("cudaFuncSetAttribute(ffma_f32 kernels): %s", cudaGetErrorString(err));
+            return err;
+        }
+        if (st.full > 0) {
+            ffma_f32_kernel<WR><<<static_cast<unsigned>(st.full), F::THREADS, F::SMEM, p.stream>>>(
+                ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status);
+            count_launch();
+        }
+        ffma_f32_split_kernel<WR><<<static_cast<unsigned>(st.rest * st.parts), F::THREADS, F::SMEM, p.stream>>>(
+            ta, tb, ws, p.m, p.n, p.k, static_cast<int>(st.full), st.parts, dev.status);
         count_launch();
     }
-    ffma_f32_split_kernel<WR><<<static_cast<unsigned>(st.rest * st.parts), F::THREADS, F::SMEM, p.stream>>>(
-        ta, tb, ws, p.m, p.n, p.k, static_cast<int>(st.full), st.parts, dev.status);
-    count_launch();
     ffma_f32_reduce_kernel<WR><<<static_cast<unsigned>(st.rest), F::THREADS, 0, p.stream>>>(
         ws, p.C, p.ldc, p.m, p.n, static_cast<int>(st.full), st.parts, vec_store);
     count_launch();
