@@ -31,10 +31,9 @@
 //    tile rows; the epilogue writes 4 rows x 128 contiguous bytes per warp
 //    instruction with 128-bit stores.
 //
-//  * Roles.  The 128-row kernel is warp-specialised: one warp group only
-//    streams tiles with TMA, two multiply, and the register file is re-split
-//    between them (setmaxnreg); the 64-row kernel used for short k keeps the
-//    producer in thread 0 of its consumers.
+//  * Roles.  The kernel is warp-specialised: one warp group only streams
+//    tiles with TMA, two multiply, and the register file is re-split between
+//    them (setmaxnreg).
 //  * The last wave.  With T = q G + r tiles on G SMs (r < 0.9 G), the one-tile
 //    grid runs the q G tiles of the full rounds and the r tiles left are cut
 //    along k into `parts` pieces that fill whole rounds best; each piece's
@@ -55,21 +54,20 @@ namespace {
 constexpr int kBN = 128;
 constexpr int kBK = 16;                  // 16 (64-byte A rows, 64-byte swizzle) or 32 (128-byte, 128-byte swizzle)
 constexpr int kStages = 4;
+constexpr int kTR = 8;                   // rows of C per consumer thread (8 or 16)
 constexpr int kRowGroup = 4;             // rows of a thread processed together (4 or 8)
 constexpr int kChunkUnroll = 4;          // unrolling of the 4-wide k chunks of a stage (1..4)
 constexpr int kGroupM = 8;
 constexpr uint32_t kStageB = kBK * kBN * 4;   // 8 KiB
 
-// WR warps stacked along M (each warp 32 rows x 64 columns, two warps across
-// N): WR = 4 gives 128 x 128 tiles and one 256-thread CTA per SM; WR = 2 gives
-// 64 x 128 tiles and two 128-thread CTAs per SM, whose barrier and prologue
-// waits overlap each other (better when k is short).
-template <int WR>
+// Eight consumer warps, four along M and two along N, each warp 4 kTR rows x
+// 64 columns: kTR = 8 gives 128 x 128 tiles.  (A 64-row form, two CTAs per
+// SM, served k < 2048 until the warp-specialised 128-row kernel beat it
+// there too: 4096 x 4096 x 1024 50.9 -> 55.6 TFLOP/s.)
 struct FCfg {
-    static constexpr int BM = 32 * WR;
-    static constexpr int THREADS = 64 * WR;
+    static constexpr int BM = 16 * kTR;
+    static constexpr int THREADS = 256;
     static constexpr int WARPS = THREADS / 32;
-    static constexpr int MIN_BLOCKS = WR == 2 ? 2 : 1;
     static constexpr uint32_t STAGE_A = BM * kBK * 4;   // 8 KiB at 128 rows
     static constexpr size_t SMEM = 1024 + kStages * (STAGE_A + kStageB) + 2 * kStages * sizeof(uint64_t);
 };
@@ -88,11 +86,11 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
 // b_col0 + 2p, +1 (p < 2) or b_col0 + 32 + 2(p-2), +1 (p >= 2) of the CTA
 // tile.  Pairs of columns are updated by one paired FMA (fma.rn.f32x2): each
 // lane is an ordinary fused multiply-add with one rounding, exactly as fmaf.
-using Acc = float2[8][4];
+using Acc = float2[kTR][4];
 
 __device__ __forceinline__ void zero(Acc& acc) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < kTR; ++i)
 #pragma unroll
         for (int p = 0; p < 4; ++p) acc[i][p] = make_float2(0.0f, 0.0f);
 }
@@ -106,7 +104,7 @@ __device__ __forceinline__ void fma_phase(Acc& acc, const float* As, const float
 #pragma unroll kChunkUnroll
     for (int kc = 0; kc < kBK / 4; ++kc) {
 #pragma unroll
-        for (int g = 0; g < 8 / kRowGroup; ++g) {
+        for (int g = 0; g < kTR / kRowGroup; ++g) {
             float4 av[kRowGroup];
 #pragma unroll
             for (int ii = 0; ii < kRowGroup; ++ii) {
@@ -140,7 +138,7 @@ __device__ __forceinline__ void fma_phase(Acc& acc, const float* As, const float
 __device__ __forceinline__ void store_tile(const Acc& acc, float* C, int64_t ldc, int M, int N, int m0, int n0,
                                            int a_row0, int b_col0, int vec_store) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kTR; ++i) {
         const int gm = m0 + a_row0 + 4 * i;
         if (gm >= M) continue;
         float* crow = C + static_cast<int64_t>(gm) * ldc;
@@ -159,9 +157,8 @@ __device__ __forceinline__ void store_tile(const Acc& acc, float* C, int64_t ldc
     }
 }
 
-// Shared-memory layout of both kernels: kStages A stages, kStages B stages,
+// Shared-memory layout: kStages A stages, kStages B stages,
 // then the full and empty mbarriers, from a 1024-byte aligned base.
-template <int WR>
 struct Smem {
     float* sA;
     float* sB;
@@ -170,8 +167,8 @@ struct Smem {
     __device__ __forceinline__ explicit Smem(uint8_t* raw) {
         uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
         sA = reinterpret_cast<float*>(base);
-        sB = reinterpret_cast<float*>(base + kStages * FCfg<WR>::STAGE_A);
-        full = reinterpret_cast<uint64_t*>(base + kStages * (FCfg<WR>::STAGE_A + kStageB));
+        sB = reinterpret_cast<float*>(base + kStages * FCfg::STAGE_A);
+        full = reinterpret_cast<uint64_t*>(base + kStages * (FCfg::STAGE_A + kStageB));
         empty = full + kStages;
     }
 };
@@ -187,7 +184,7 @@ struct Smem {
 // parts == 1, tile tile0 + u and stores it in C; with parts > 1, piece
 // u % parts (k-phases [KT p / parts, KT (p + 1) / parts)) of tile
 // tile0 + u / parts, whose partial sums go to slot u of `ws` (float4 j of
-// consumer thread t at j * 256 + t) for ffma_f32_reduce_kernel<4>.
+// consumer thread t at j * 256 + t) for ffma_f32_reduce_kernel.
 constexpr int kWsThreads = 384;
 constexpr int kProducerRegs = 24, kConsumerRegs = 240;
 static_assert(128 * kProducerRegs + 256 * kConsumerRegs <= 65536, "register split exceeds the file");
@@ -196,10 +193,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    float* __restrict__ C, int64_t ldc, int M, int N, int K, int vec_store, uint32_t* status,
                    int tile0, int parts, float* __restrict__ ws) {
-    using F = FCfg<4>;
+    using F = FCfg;
     constexpr int kBM = F::BM;
     extern __shared__ uint8_t smem_raw[];
-    const Smem<4> sm(smem_raw);
+    const Smem sm(smem_raw);
     const int warp_all = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // Tile origin and k-range of this block (recomputed where needed rather
@@ -251,12 +248,12 @@ ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kConsumerRegs));
     const int ctid = threadIdx.x - 128;
     const int warp = ctid >> 5;
-    // Thread layout: warp (wm, wn) covers rows 32*wm .. +31 and columns
-    // 64*wn .. +63; lane (tm, tn) takes rows tm + 4i (i < 8) and columns
+    // Thread layout: warp (wm, wn) covers rows 4 kTR wm .. + 4 kTR - 1 and
+    // columns 64*wn .. +63; lane (tm, tn) takes rows tm + 4i (i < kTR) and columns
     // 4*tn .. +3 and 32 + 4*tn .. +3 of that warp tile.
     const int wm = warp >> 1, wn = warp & 1;
     const int tm = lane >> 3, tn = lane & 7;
-    const int a_row0 = 32 * wm + tm;
+    const int a_row0 = 4 * kTR * wm + tm;
     const int b_col0 = 64 * wn + 4 * tn;
     // 64-byte swizzle: 16-byte chunk c of tile row r sits at chunk c ^ ((r >> 1) & 3).
     // For r = a_row0 + 4i this is (tm >> 1) ^ (2 * (i & 1)).
@@ -282,181 +279,23 @@ ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
     float4* dst = reinterpret_cast<float4*>(ws + static_cast<int64_t>(blockIdx.x) * kBM * kBN) + ctid;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < kTR; ++i)
 #pragma unroll
         for (int p = 0; p < 4; p += 2)
             dst[(i * 2 + p / 2) * F::THREADS] = make_float4(acc[i][p].x, acc[i][p].y, acc[i][p + 1].x, acc[i][p + 1].y);
 }
 
-// Data-parallel form: one CTA per C tile, which walks all of its k-phases.
-template <int WR>
-__global__ void __launch_bounds__(FCfg<WR>::THREADS, FCfg<WR>::MIN_BLOCKS)
-ffma_f32_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                float* __restrict__ C, int64_t ldc, int M, int N, int K, int vec_store, uint32_t* status) {
-    using F = FCfg<WR>;
-    constexpr int kBM = F::BM;
-    extern __shared__ uint8_t smem_raw[];
-    const Smem<WR> sm(smem_raw);
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    int tile_m, tile_n;
-    tile_coords(blockIdx.x, (M + kBM - 1) / kBM, (N + kBN - 1) / kBN, tile_m, tile_n);
-    const int m0 = tile_m * kBM;
-    const int n0 = tile_n * kBN;
-    const int KT = (K + kBK - 1) / kBK;
-
-    auto issue = [&](int slot, int kt) {
-        mbar_arrive_expect_tx(&sm.full[slot], F::STAGE_A + kStageB);
-        tma_load_2d(sm.sA + slot * (kBM * kBK), &tmA, &sm.full[slot], kt * kBK, m0);
-        tma_load_2d(sm.sB + slot * (kBK * kBN), &tmB, &sm.full[slot], n0, kt * kBK);
-    };
-    if (tid == 0) {
-        tma_prefetch_map(&tmA);
-        tma_prefetch_map(&tmB);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], F::WARPS);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
-    if (tid == 0)
-        for (int s = 0; s < min(KT, kStages); ++s) issue(s, s);
-
-    // Thread layout: warp (wm, wn) covers rows 32*wm .. +31 and columns
-    // 64*wn .. +63; lane (tm, tn) takes rows tm + 4i (i < 8) and columns
-    // 4*tn .. +3 and 32 + 4*tn .. +3 of that warp tile.
-    const int wm = warp >> 1, wn = warp & 1;
-    const int tm = lane >> 3, tn = lane & 7;
-    const int a_row0 = 32 * wm + tm;
-    const int b_col0 = 64 * wn + 4 * tn;
-    // 64-byte swizzle: 16-byte chunk c of tile row r sits at chunk c ^ ((r >> 1) & 3).
-    // For r = a_row0 + 4i this is (tm >> 1) ^ (2 * (i & 1)).
-    // 128-byte swizzle (kBK = 32): chunk c of tile row r sits at c ^ (r & 7),
-    // which for r = a_row0 + 4i is tm ^ (4 * (i & 1)).
-    const int swz_even = kBK == 16 ? (tm >> 1) : tm;
-
-    Acc acc;
-    zero(acc);
-    bool ok = true;
-    int s = 0;
-    uint32_t phase = 0;
-    for (int kt = 0; kt < KT; ++kt) {
-        // Refill the stage drained in the previous phase with phase kt-1+kStages.
-        if (tid == 0 && kt > 0) {
-            const int next = kt - 1 + kStages;
-            if (next < KT) {
-                const int ps = (kt - 1) % kStages;
-                const uint32_t pph = static_cast<uint32_t>((kt - 1) / kStages) & 1u;
-                if (!mbar_wait(&sm.empty[ps], pph, status)) { ok = false; break; }
-                issue(ps, next);
-            }
-        }
-        if (!mbar_wait(&sm.full[s], phase, status)) { ok = false; break; }
-        fma_phase(acc, sm.sA + s * (kBM * kBK), sm.sB + s * (kBK * kBN), a_row0, b_col0, swz_even);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[s]);
-        if (++s == kStages) { s = 0; phase ^= 1u; }
-    }
-    if (!ok) return;   // status already records the timeout; C is left unwritten
-    store_tile(acc, C, ldc, M, N, m0, n0, a_row0, b_col0, vec_store);
-}
-
-// Remainder tiles cut along k ("split-K"): block u computes part u % parts of
-// tile tile0 + u / parts -- k-phases [KT part / parts, KT (part + 1) / parts)
-// -- with the data-parallel kernel's pipeline and stores its partial sums in
-// slot u of `ws` (float4 j of thread t at j * THREADS + t, so a warp stores
-// 512 contiguous bytes).
-template <int WR>
-__global__ void __launch_bounds__(FCfg<WR>::THREADS, FCfg<WR>::MIN_BLOCKS)
-ffma_f32_split_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      float* __restrict__ ws, int M, int N, int K, int tile0, int parts, uint32_t* status) {
-    using F = FCfg<WR>;
-    constexpr int kBM = F::BM;
-    extern __shared__ uint8_t smem_raw[];
-    const Smem<WR> sm(smem_raw);
-
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5;
-    const int lane = tid & 31;
-    const int u = blockIdx.x, part = u % parts;
-    int tile_m, tile_n;
-    tile_coords(tile0 + u / parts, (M + kBM - 1) / kBM, (N + kBN - 1) / kBN, tile_m, tile_n);
-    const int m0 = tile_m * kBM;
-    const int n0 = tile_n * kBN;
-    const int KT = (K + kBK - 1) / kBK;
-    const int k0 = static_cast<int>(static_cast<int64_t>(KT) * part / parts);
-    const int NI = static_cast<int>(static_cast<int64_t>(KT) * (part + 1) / parts) - k0;
-
-    auto issue = [&](int slot, int i) {
-        mbar_arrive_expect_tx(&sm.full[slot], F::STAGE_A + kStageB);
-        tma_load_2d(sm.sA + slot * (kBM * kBK), &tmA, &sm.full[slot], (k0 + i) * kBK, m0);
-        tma_load_2d(sm.sB + slot * (kBK * kBN), &tmB, &sm.full[slot], n0, (k0 + i) * kBK);
-    };
-    if (tid == 0) {
-        tma_prefetch_map(&tmA);
-        tma_prefetch_map(&tmB);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], F::WARPS);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
-    if (tid == 0)
-        for (int s = 0; s < min(NI, kStages); ++s) issue(s, s);
-
-    // Thread layout and swizzle as in the data-parallel kernel.
-    const int wm = warp >> 1, wn = warp & 1;
-    const int tm = lane >> 3, tn = lane & 7;
-    const int a_row0 = 32 * wm + tm;
-    const int b_col0 = 64 * wn + 4 * tn;
-    const int swz_even = kBK == 16 ? (tm >> 1) : tm;
-
-    Acc acc;
-    zero(acc);
-    bool ok = true;
-    int s = 0;
-    uint32_t phase = 0;
-    for (int i = 0; i < NI; ++i) {
-        if (tid == 0 && i > 0) {
-            const int next = i - 1 + kStages;
-            if (next < NI) {
-                const int ps = (i - 1) % kStages;
-                const uint32_t pph = static_cast<uint32_t>((i - 1) / kStages) & 1u;
-                if (!mbar_wait(&sm.empty[ps], pph, status)) { ok = false; break; }
-                issue(ps, next);
-            }
-        }
-        if (!mbar_wait(&sm.full[s], phase, status)) { ok = false; break; }
-        fma_phase(acc, sm.sA + s * (kBM * kBK), sm.sB + s * (kBK * kBN), a_row0, b_col0, swz_even);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[s]);
-        if (++s == kStages) { s = 0; phase ^= 1u; }
-    }
-    if (!ok) return;   // status records the timeout
-    float4* dst = reinterpret_cast<float4*>(ws + static_cast<int64_t>(u) * kBM * kBN) + tid;
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int p = 0; p < 4; p += 2)
-            dst[(i * 2 + p / 2) * F::THREADS] = make_float4(acc[i][p].x, acc[i][p].y, acc[i][p + 1].x, acc[i][p + 1].y);
-}
-
-// C of the remainder tiles: tile tile0 + b is the sum of the split kernel's
+// C of the remainder tiles: tile tile0 + b is the sum of the pieces in
 // slots b * parts .. b * parts + parts - 1, added in part order.
-template <int WR>
-__global__ void __launch_bounds__(FCfg<WR>::THREADS)
+__global__ void __launch_bounds__(FCfg::THREADS)
 ffma_f32_reduce_kernel(const float* __restrict__ ws, float* __restrict__ C, int64_t ldc, int M, int N, int tile0,
                        int parts, int vec_store) {
-    using F = FCfg<WR>;
+    using F = FCfg;
     constexpr int kBM = F::BM;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int wm = warp >> 1, wn = warp & 1;
     const int tm = lane >> 3, tn = lane & 7;
-    const int a_row0 = 32 * wm + tm;
+    const int a_row0 = 4 * kTR * wm + tm;
     const int b_col0 = 64 * wn + 4 * tn;
     int tile_m, tile_n;
     tile_coords(tile0 + blockIdx.x, (M + kBM - 1) / kBM, (N + kBN - 1) / kBN, tile_m, tile_n);
@@ -465,7 +304,7 @@ ffma_f32_reduce_kernel(const float* __restrict__ ws, float* __restrict__ C, int6
     const float4* src = reinterpret_cast<const float4*>(ws + static_cast<int64_t>(blockIdx.x) * parts * kBM * kBN) + tid;
     for (int q = 0; q < parts; ++q) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < kTR; ++i)
 #pragma unroll
             for (int p = 0; p < 4; p += 2) {
                 const float4 v = __ldcs(src + (i * 2 + p / 2) * F::THREADS);
@@ -483,69 +322,42 @@ ffma_f32_reduce_kernel(const float* __restrict__ ws, float* __restrict__ C, int6
 cudaError_t launch_ws(const Problem& p, const CUtensorMap& ta, const CUtensorMap& tb, int64_t grid, int64_t tile0,
                       int parts, float* ws, int vec_store, const Device& dev) {
     cudaError_t err = cudaFuncSetAttribute(ffma_f32_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(FCfg<4>::SMEM));
+                                           static_cast<int>(FCfg::SMEM));
     if (err != cudaSuccess) {
         set_error("cudaFuncSetAttribute(ffma_f32_ws_kernel): %s", cudaGetErrorString(err));
         return err;
     }
-    ffma_f32_ws_kernel<<<static_cast<unsigned>(grid), kWsThreads, FCfg<4>::SMEM, p.stream>>>(
+    ffma_f32_ws_kernel<<<static_cast<unsigned>(grid), kWsThreads, FCfg::SMEM, p.stream>>>(
         ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status, static_cast<int>(tile0), parts, ws);
     count_launch();
     return cudaSuccess;
 }
 
-// Launches the one-tile-per-CTA kernel over all tiles.
-template <int WR>
-cudaError_t launch_wr(const Problem& p, const Device& dev) {
-    using F = FCfg<WR>;
-    CUtensorMap ta, tb;
-    if (!make_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.A, p.m, p.k, p.lda, F::BM, kBK,
-                         kBK == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.k, p.n, p.ldb, kBK, kBN,
-                         CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    const int64_t tiles = static_cast<int64_t>((p.m + F::BM - 1) / F::BM) * ((p.n + kBN - 1) / kBN);
-    const int vec_store = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
-    cudaError_t err;
-    if constexpr (WR == 4) {
-        err = launch_ws(p, ta, tb, tiles, 0, 1, nullptr, vec_store, dev);
-    } else {
-        err = cudaFuncSetAttribute(ffma_f32_kernel<WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(F::SMEM));
-        if (err != cudaSuccess) {
-            set_error("cudaFuncSetAttribute(ffma_f32_kernel): %s", cudaGetErrorString(err));
-            return err;
-        }
-        ffma_f32_kernel<WR><<<static_cast<unsigned>(tiles), F::THREADS, F::SMEM, p.stream>>>(
-            ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status);
-        count_launch();
-    }
-    if (err == cudaSuccess) err = cudaGetLastError();
-    if (err != cudaSuccess) set_error("ffma_f32_kernel launch: %s", cudaGetErrorString(err));
-    return err;
+bool make_maps(const Problem& p, CUtensorMap* ta, CUtensorMap* tb) {
+    using F = FCfg;
+    return make_tensor_map(ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.A, p.m, p.k, p.lda, F::BM, kBK,
+                           kBK == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_tensor_map(tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.k, p.n, p.ldb, kBK, kBN,
+                           CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-// Measured on GB300: 4096^3 53.2 TFLOP/s with 128-row CTAs vs 52.6 with two
-// 64-row CTAs per SM; 4097 x 3001 x 1024 42.8 vs 46.3.
-constexpr int kShortK = 2048;
+int vec_store_ok(const Problem& p) { return (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0); }
 
-// Split remainder: the one-tile grid runs the tiles of its full rounds (G
-// slots a round: SMs x resident CTAs per SM); the r tiles left (r < 0.9 G)
-// are cut along k into `parts` pieces, chosen so that r * parts pieces fill
-// whole rounds best (each round of pieces takes 1/parts of a tile's time); a
-// reduce kernel adds the pieces.  4096^3 (128-row tiles, 152 slots): 1024 =
-// 6 x 152 + 112 tiles; 112 x 4 quarters = 2.95 rounds of quarter tiles
-// instead of one round of whole tiles.
+// Split remainder: the kernel runs the tiles of the full rounds (152 a round
+// on GB300); the r tiles left (r < 0.9 G) are cut along k into `parts`
+// pieces, chosen so that r * parts pieces fill whole rounds best (each round
+// of pieces takes 1/parts of a tile's time); a reduce kernel adds the pieces.
+// 4096^3: 1024 = 6 x 152 + 112 tiles; 112 x 4 quarters = 2.95 rounds of
+// quarter tiles instead of one round of whole tiles.
 struct SplitTail {
-    int64_t full;   // tiles of the full rounds (one-tile grid)
+    int64_t full;   // tiles of the full rounds
     int64_t rest;   // remainder tiles
     int parts;
 };
 
-template <int WR>
 bool split_tail(const Problem& p, const Device& dev, SplitTail* st) {
-    using F = FCfg<WR>;
-    const int64_t G = static_cast<int64_t>(dev.sm_count) * F::MIN_BLOCKS;
+    using F = FCfg;
+    const int64_t G = dev.sm_count;
     const int64_t tiles = static_cast<int64_t>((p.m + F::BM - 1) / F::BM) * ((p.n + kBN - 1) / kBN);
     const int64_t KT = (p.k + kBK - 1) / kBK;
     const int64_t r = tiles % G;
@@ -564,46 +376,32 @@ bool split_tail(const Problem& p, const Device& dev, SplitTail* st) {
     return true;
 }
 
-template <int WR>
+cudaError_t launch_tiles(const Problem& p, const Device& dev) {
+    using F = FCfg;
+    CUtensorMap ta, tb;
+    if (!make_maps(p, &ta, &tb)) return cudaErrorInvalidValue;
+    const int64_t tiles = static_cast<int64_t>((p.m + F::BM - 1) / F::BM) * ((p.n + kBN - 1) / kBN);
+    cudaError_t err = launch_ws(p, ta, tb, tiles, 0, 1, nullptr, vec_store_ok(p), dev);
+    if (err == cudaSuccess) err = cudaGetLastError();
+    if (err != cudaSuccess) set_error("ffma_f32_ws_kernel launch: %s", cudaGetErrorString(err));
+    return err;
+}
+
 cudaError_t launch_split_tail(const Problem& p, const Device& dev, void* workspace, const SplitTail& st) {
-    using F = FCfg<WR>;
+    using F = FCfg;
     if (!workspace) {
         set_error("ffma_f32: split remainder launched without its workspace");
         return cudaErrorInvalidValue;
     }
     CUtensorMap ta, tb;
-    if (!make_tensor_map(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.A, p.m, p.k, p.lda, F::BM, kBK,
-                         kBK == 16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.B, p.k, p.n, p.ldb, kBK, kBN,
-                         CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    const int vec_store = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
+    if (!make_maps(p, &ta, &tb)) return cudaErrorInvalidValue;
+    const int vec_store = vec_store_ok(p);
     float* ws = static_cast<float*>(workspace);
     cudaError_t err = cudaSuccess;
-    if constexpr (WR == 4) {
-        if (st.full > 0) err = launch_ws(p, ta, tb, st.full, 0, 1, nullptr, vec_store, dev);
-        if (err == cudaSuccess) err = launch_ws(p, ta, tb, st.rest * st.parts, st.full, st.parts, ws, vec_store, dev);
-        if (err != cudaSuccess) return err;
-    } else {
-        err = cudaFuncSetAttribute(ffma_f32_kernel<WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   static_cast<int>(F::SMEM));
-        if (err == cudaSuccess)
-            err = cudaFuncSetAttribute(ffma_f32_split_kernel<WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(F::SMEM));
-        if (err != cudaSuccess) {
-            set_error("cudaFuncSetAttribute(ffma_f32 kernels): %s", cudaGetErrorString(err));
-            return err;
-        }
-        if (st.full > 0) {
-            ffma_f32_kernel<WR><<<static_cast<unsigned>(st.full), F::THREADS, F::SMEM, p.stream>>>(
-                ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status);
-            count_launch();
-        }
-        ffma_f32_split_kernel<WR><<<static_cast<unsigned>(st.rest * st.parts), F::THREADS, F::SMEM, p.stream>>>(
-            ta, tb, ws, p.m, p.n, p.k, static_cast<int>(st.full), st.parts, dev.status);
-        count_launch();
-    }
-    ffma_f32_reduce_kernel<WR><<<static_cast<unsigned>(st.rest), F::THREADS, 0, p.stream>>>(
+    if (st.full > 0) err = launch_ws(p, ta, tb, st.full, 0, 1, nullptr, vec_store, dev);
+    if (err == cudaSuccess) err = launch_ws(p, ta, tb, st.rest * st.parts, st.full, st.parts, ws, vec_store, dev);
+    if (err != cudaSuccess) return err;
+    ffma_f32_reduce_kernel<<<static_cast<unsigned>(st.rest), F::THREADS, 0, p.stream>>>(
         ws, p.C, p.ldc, p.m, p.n, static_cast<int>(st.full), st.parts, vec_store);
     count_launch();
     err = cudaGetLastError();
@@ -615,15 +413,13 @@ cudaError_t launch_split_tail(const Problem& p, const Device& dev, void* workspa
 
 uint64_t ffma_f32_workspace_bytes(const Problem& p, const Device& dev) {
     SplitTail st;
-    if (p.k < kShortK)
-        return split_tail<2>(p, dev, &st) ? static_cast<uint64_t>(st.rest) * st.parts * FCfg<2>::BM * kBN * 4 : 0;
-    return split_tail<4>(p, dev, &st) ? static_cast<uint64_t>(st.rest) * st.parts * FCfg<4>::BM * kBN * 4 : 0;
+    if (!split_tail(p, dev, &st)) return 0;
+    return static_cast<uint64_t>(st.rest) * st.parts * FCfg::BM * kBN * sizeof(float);
 }
 
 cudaError_t launch_ffma_f32(const Problem& p, const Device& dev, void* workspace) {
     SplitTail st;
-    if (p.k < kShortK) return split_tail<2>(p, dev, &st) ? launch_split_tail<2>(p, dev, workspace, st) : launch_wr<2>(p, dev);
-    return split_tail<4>(p, dev, &st) ? launch_split_tail<4>(p, dev, workspace, st) : launch_wr<4>(p, dev);
+    return split_tail(p, dev, &st) ? launch_split_tail(p, dev, workspace, st) : launch_tiles(p, dev);
 }
 
 }  // namespace tgemm

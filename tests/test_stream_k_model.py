@@ -28,11 +28,9 @@ import pytest
 BM, BN, BK = 128, 128, 16
 
 
-def split_tail(m, n, k, sm_count=152, short_k=2048, stages=4):
-    """(full-round tiles, remainder tiles, parts) of the fp32 launcher, or None.
-    k < short_k: 64-row tiles, two blocks per SM; else 128-row tiles, one."""
-    bm, G = (64, 2 * sm_count) if k < short_k else (128, sm_count)
-    tiles = -(-m // bm) * -(-n // BN)
+def split_tail(m, n, k, G=152, stages=4):
+    """(full-round tiles, remainder tiles, parts) of the fp32 launcher, or None."""
+    tiles = -(-m // BM) * -(-n // BN)
     kt = -(-k // BK)
     r = tiles % G
     if r == 0 or 10 * r >= 9 * G:
@@ -51,8 +49,8 @@ def test_split_tail_choices():
     assert split_tail(4096, 4096, 4096) == (912, 112, 4)      # 112 x 4 quarters = 2.95 rounds
     assert split_tail(1024, 1024, 4096) == (0, 64, 7)          # less than one wave: all split
     assert split_tail(8192, 8192, 2048) is None                # 4096 tiles: last round 95 % full
-    assert split_tail(4097, 3001, 1023) == (1520, 40, 7)       # 64-row tiles, 304 slots a round
-    assert split_tail(8192, 8192, 512) is None                 # 8192 64-row tiles: no remainder
+    assert split_tail(4097, 3001, 1023) == (760, 32, 4)        # 792 tiles: 5 rounds + 32
+    assert split_tail(8192, 8192, 512) is None                 # 4096 tiles: last round 95 % full
     assert split_tail(200, 150, 90) is None                    # 6 k-phases: too short to cut
     assert split_tail(256, 256, 65536) == (0, 4, 8)            # 4 tiles, 4096 phases: 8 pieces each
     for shape in [(2432, 2100, 2050), (1000, 900, 4100), (500, 20000, 2050), (2000, 2000, 4100)]:
