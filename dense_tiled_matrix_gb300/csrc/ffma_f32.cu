@@ -9,7 +9,7 @@
 //    rows so that CTAs running together share A and B tiles in L2.
 //  * Phases.  K is walked in phases of BK = 16.  Instead of every thread
 //    copying one element and a __syncthreads, one thread issues two TMA bulk
-//    tensor copies per phase into a 4-stage ring of shared-memory tiles; an
+//    tensor copies per phase into an 8-stage ring of shared-memory tiles; an
 //    mbarrier per stage ("full") replaces the first __syncthreads (data has
 //    landed) and a second per stage ("empty", one arrival per warp) replaces
 //    the second one (nobody still reads the tile that the next copy
@@ -53,7 +53,7 @@ namespace {
 
 constexpr int kBN = 128;
 constexpr int kBK = 16;                  // 16 (64-byte A rows, 64-byte swizzle) or 32 (128-byte, 128-byte swizzle)
-constexpr int kStages = 4;
+constexpr int kStages = 8;               // 4 -> 8: 57.8 -> 59.0 TFLOP/s at 4096^3
 constexpr int kTR = 8;                   // rows of C per consumer thread (8 or 16)
 constexpr int kRowGroup = 4;             // rows of a thread processed together (4 or 8)
 constexpr int kChunkUnroll = 4;          // unrolling of the 4-wide k chunks of a stage (1..4)

@@ -28,7 +28,7 @@ import pytest
 BM, BN, BK = 128, 128, 16
 
 
-def split_tail(m, n, k, G=152, stages=4):
+def split_tail(m, n, k, G=152, stages=8):
     """(full-round tiles, remainder tiles, parts) of the fp32 launcher, or None."""
     tiles = -(-m // BM) * -(-n // BN)
     kt = -(-k // BK)
@@ -63,14 +63,14 @@ def test_split_tail_covers_every_phase_once(shape):
     m, n, k = shape
     full, rest, parts = split_tail(m, n, k)
     kt = -(-k // BK)
-    assert kt // parts >= 8
+    assert kt // parts >= 16
     tiles = full + rest
     done = np.zeros((tiles, kt), dtype=np.int64)
     done[:full] += 1                                           # one-tile grid: blocks 0 .. full-1
     for u in range(rest * parts):                              # split kernel: block u -> slot u
         t, part = full + u // parts, u % parts
         k0, k1 = kt * part // parts, kt * (part + 1) // parts
-        assert k1 - k0 >= 7
+        assert k1 - k0 >= 16
         done[t, k0:k1] += 1
     assert (done == 1).all()
     # reduce block b reads slots b * parts .. b * parts + parts - 1, all written
