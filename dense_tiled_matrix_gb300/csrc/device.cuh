@@ -79,6 +79,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     }
 }
 
+// A CTA must not exit while a bulk copy it issued may still write its shared
+// memory or signal its barriers.  On the normal path every copy has been
+// waited for by the time a producer gets here; after a timeout some may not
+// have been.  `issued` copies (or groups of copies) went out in ring order --
+// number i into stage i mod `stages`, completing phase i / stages of full[s]
+// -- and this waits, each wait bounded by `limit_ns`, for the last phase
+// armed on every stage.
+constexpr uint64_t kDrainLimitNs = 200000000ull;   // 200 ms per stage
+__device__ __forceinline__ void drain_ring(uint64_t* full, int stages, int issued, uint32_t* status) {
+#pragma unroll 1
+    for (int s = 0; s < stages && s < issued; ++s) {
+        const int fills = issued / stages + (s < issued % stages ? 1 : 0);
+        mbar_wait(&full[s], static_cast<uint32_t>(fills - 1) & 1u, status, kDrainLimitNs);
+    }
+}
+
+// Rounds a dynamic shared-memory pointer up to a 1024-byte boundary (the
+// alignment of 128-byte-swizzled TMA tiles) by pointer arithmetic on the
+// pointer itself.  Rounding through an integer cast hides from the compiler
+// that the result still points into shared memory, and every access through
+// it becomes a generic load or store (measured on GB300: the FFMA kernel's
+// shared-memory operand reads, 59.1 -> 63.5 TFLOP/s at 4096^3 once they were
+// shared loads again).
+__device__ __forceinline__ uint8_t* smem_align_1024(uint8_t* raw) {
+    return raw + ((1024u - static_cast<uint32_t>(reinterpret_cast<uintptr_t>(raw) & 1023u)) & 1023u);
+}
+
 // --------------------------------------------------------------------- TMA --
 
 __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {

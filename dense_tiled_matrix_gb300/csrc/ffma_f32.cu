@@ -165,7 +165,7 @@ struct Smem {
     uint64_t* full;
     uint64_t* empty;
     __device__ __forceinline__ explicit Smem(uint8_t* raw) {
-        uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+        uint8_t* base = smem_align_1024(raw);
         sA = reinterpret_cast<float*>(base);
         sB = reinterpret_cast<float*>(base + kStages * FCfg::STAGE_A);
         full = reinterpret_cast<uint64_t*>(base + kStages * (FCfg::STAGE_A + kStageB));
@@ -232,6 +232,7 @@ ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             int m0, n0, k0, NI;
             origin(m0, n0);
             k_range(k0, NI);
+            int issued = 0;
             for (int i = 0; i < NI; ++i) {
                 const int s = i % kStages;
                 if (i >= kStages && !mbar_wait(&sm.empty[s], static_cast<uint32_t>(i / kStages - 1) & 1u, status))
@@ -239,7 +240,11 @@ ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 mbar_arrive_expect_tx(&sm.full[s], F::STAGE_A + kStageB);
                 tma_load_2d(sm.sA + s * (kBM * kBK), &tmA, &sm.full[s], (k0 + i) * kBK, m0);
                 tma_load_2d(sm.sB + s * (kBK * kBN), &tmB, &sm.full[s], n0, (k0 + i) * kBK);
+                issued = i + 1;
             }
+            // This thread keeps the CTA alive until its copies have landed
+            // (consumers that timed out may have left some unwaited).
+            drain_ring(sm.full, kStages, issued, status);
         }
         return;
     }

@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kXThreads, 2)
 transpose_tma_kernel(const __grid_constant__ CUtensorMap tm_src, const __grid_constant__ CUtensorMap tm_dst,
                      int rows, int cols, uint32_t* status) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* base = smem_align_1024(smem_raw);
     uint8_t* in = base;                                           // kXStages swizzled input tiles
     float* out = reinterpret_cast<float*>(base + kXStages * kXTileBytes);   // 2 x [kXC][kXR]
     uint64_t* full = reinterpret_cast<uint64_t*>(base + (kXStages + 2) * kXTileBytes);
@@ -83,12 +83,14 @@ transpose_tma_kernel(const __grid_constant__ CUtensorMap tm_src, const __grid_co
         tma_load_2d(in + s * kXTileBytes, &tm_src, &full[s], static_cast<int>(t % tiles_c) * kXC,
                     static_cast<int>(t / tiles_c) * kXR);
     };
+    int issued = 0;   // loads issued (thread 0)
     if (tid == 0) {
         tma_prefetch_map(&tm_src);
         tma_prefetch_map(&tm_dst);
         for (int s = 0; s < kXStages; ++s) mbar_init(&full[s], 1);
         fence_barrier_init();
         for (int i = 0; i < n && i < kXStages; ++i) load(i);
+        issued = n < kXStages ? n : kXStages;
     }
     __syncthreads();
 
@@ -123,10 +125,14 @@ transpose_tma_kernel(const __grid_constant__ CUtensorMap tm_src, const __grid_co
             if (ok && i + kXStages < n) {
                 fence_proxy_async_smem();
                 load(i + kXStages);
+                ++issued;
             }
         }
     }
-    if (tid == 0) bulk_wait_group<0>();
+    if (tid == 0) {
+        drain_ring(full, kXStages, issued, status);   // loads left unwaited after a timeout
+        bulk_wait_group<0>();
+    }
 }
 
 }  // namespace

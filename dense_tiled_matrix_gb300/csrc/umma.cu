@@ -103,8 +103,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             float* __restrict__ ws, unsigned* __restrict__ flags) {
     using G = Cfg<kTF32, kBKMajor, kWide, kBN>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
+    uint8_t* smem = smem_align_1024(smem_raw);
     uint8_t* sA = smem;
     uint8_t* sB = smem + G::STAGES * G::A_BYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(sB + G::STAGES * G::B_BYTES);
@@ -170,6 +169,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
+            int issued = 0;
             Seq sq;
             seq_init(sq);
             int tile, ka, kz;
@@ -189,9 +189,11 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                             tma_load_2d(b_dst + c * G::CH_BYTES, &tmB, &full[s], tn * G::BN + c * G::CH,
                                         kb * G::BK);
                     }
+                    ++issued;
                     if (++s == G::STAGES) { s = 0; ph ^= 1u; }
                 }
             }
+            drain_ring(full, G::STAGES, issued, status);   // no copy outlives the CTA
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
@@ -200,6 +202,8 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             uint32_t ph = 0;
             bool ok = true;
             int it = 0;
+            int last_s = -1;   // stage of the last commit to an empty barrier
+            uint32_t last_ph = 0;
             Seq sq;
             seq_init(sq);
             int tile, ka, kz;
@@ -236,11 +240,16 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         }
                     }
                     umma_commit(&empty[s]);   // stage free once these MMAs complete
+                    last_s = s;
+                    last_ph = ph;
                     if (++s == G::STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (!ok) break;
                 umma_commit(&acc_full[acc]);  // accumulator ready for the epilogue
             }
+            // The last commit completes once every MMA issued before it has:
+            // none may still run when the tensor memory is freed.
+            if (last_s >= 0) mbar_wait(&empty[last_s], last_ph, status, kDrainLimitNs);
         }
     } else {
         // --------------------------------------------------- epilogue --

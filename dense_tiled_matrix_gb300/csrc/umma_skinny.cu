@@ -65,8 +65,7 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                    uint32_t* status) {
     using G = SkinnyCfg<NM, NT>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                               ~uintptr_t(1023));
+    uint8_t* smem = smem_align_1024(smem_raw);
     uint8_t* sB = smem;                                   // STAGES x 16 KiB
     uint8_t* sA = smem + G::STAGES * G::STAGE_B;            // STAGES x NM*128 B
     uint64_t* full = reinterpret_cast<uint64_t*>(sA + G::STAGES * G::STAGE_A);
@@ -121,15 +120,20 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         // ---------------------------------------------------- TMA producer --
         int s = prefill % G::STAGES;
         uint32_t ph = prefill == G::STAGES ? 1u : 0u;
+        int issued = prefill;
         for (int kb = kb0 + prefill; kb < kb1; ++kb) {
             if (!mbar_wait(&empty[s], ph ^ 1u, status)) { ok = false; break; }
             issue(s, kb);
+            ++issued;
             if (++s == G::STAGES) { s = 0; ph ^= 1u; }
         }
+        drain_ring(full, G::STAGES, issued, status);   // no copy outlives the CTA
     } else if (warp == 1 && lane == 0) {
         // ----------------------------------------------------- MMA issuer --
         int s = 0;
         uint32_t ph = 0;
+        int last_s = -1;   // stage of the last commit to an empty barrier
+        uint32_t last_ph = 0;
         for (int i = 0; i < nkb; ++i) {
             if (!mbar_wait(&full[s], ph, status)) { ok = false; break; }
             tc_fence_after_sync();
@@ -149,9 +153,14 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 }
             }
             umma_commit(&empty[s]);
+            last_s = s;
+            last_ph = ph;
             if (++s == G::STAGES) { s = 0; ph ^= 1u; }
         }
         if (ok) umma_commit(done);
+        // The last commit completes once every MMA issued before it has:
+        // none may still run when the tensor memory is freed.
+        if (last_s >= 0) mbar_wait(&empty[last_s], last_ph, status, kDrainLimitNs);
     }
 
     // ------------------------------------- partial sums -> shared memory --
