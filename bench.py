@@ -68,8 +68,8 @@ SLOW_EXTRA_ITERS = 4   # timed launches of the pages' kernels (tens of ms each)
 # re-taken whenever that kernel changes; shapes without an entry report null.
 NCU_TRAFFIC = {
     "f32_4096": (457.87e6, "profiles/ffma_f32_4096.md (the three launches of one tgemm_f32 call)"),
-    "bf16_8192": (1112.75e6, "profiles/umma_bf16_8192.md (umma_kernel<0, 0, 1, 256, 0>)"),
-    "tf32_4096": (237.42e6, "profiles/umma_tf32_4096.md (umma_kernel<1, 1, 1, 224, 0>, without the B transpose)"),
+    "bf16_8192": (1112.98e6, "profiles/umma_bf16_8192.md (umma_kernel<0, 0, 1, 256, 0>)"),
+    "tf32_4096": (237.49e6, "profiles/umma_tf32_4096.md (umma_kernel<1, 1, 1, 224, 0>, without the B transpose)"),
 }
 KERNEL_NAMES = {"f32": "ffma_f32_ws_kernel (912 tiles, then 448 split pieces) + ffma_f32_reduce_kernel (one tgemm_f32 call)", "tf32": "umma_kernel<1, 1, 1, 224, 0>", "bf16": "umma_kernel<0, 0, 1, 256, 0>"}
 

@@ -55,7 +55,7 @@ constexpr int kBN = 128;
 constexpr int kBK = 16;                  // 16 (64-byte A rows, 64-byte swizzle) or 32 (128-byte, 128-byte swizzle)
 constexpr int kStages = 8;               // 4 -> 8: 57.8 -> 59.0 TFLOP/s at 4096^3
 constexpr int kTR = 8;                   // rows of C per consumer thread (8 or 16)
-constexpr int kRowGroup = 4;             // rows of a thread processed together (4 or 8)
+constexpr int kRowGroup = 8;             // rows of a thread processed together (4 or 8)
 constexpr int kChunkUnroll = 4;          // unrolling of the 4-wide k chunks of a stage (1..4)
 constexpr int kGroupM = 8;
 constexpr uint32_t kStageB = kBK * kBN * 4;   // 8 KiB
