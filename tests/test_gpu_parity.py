@@ -242,3 +242,19 @@ def test_full_size_8192_bf16():
 
 def test_skinny_16x8192x8192_bf16():
     parity.full_check("bf16", inputs.make("skinny"))
+
+
+# bf16 with m <= 64 takes the transposed cluster kernel: 16-, 32- and 64-row
+# forms (m <= 16, <= 32, <= 64), k split over 1..8 CTAs of a cluster, ragged
+# column tiles and k tails, and a k-slice count that does not divide k.
+SKINNY_SHAPES = [(16, 128, 64), (17, 300, 200), (24, 1000, 4100), (32, 1000, 8192), (33, 129, 70),
+                 (48, 2000, 1000), (63, 8200, 130), (64, 4096, 8192), (3, 20000, 4160)]
+
+
+@pytest.mark.parametrize("shape", SKINNY_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_skinny_bf16_row_forms(shape):
+    m, n, k = shape
+    parity.full_check("bf16", inputs.random_case(5000 + m + 7 * n + 13 * k, m, n, k, kind="int"),
+                      f"bf16 skinny int {shape}")
+    parity.full_check("bf16", inputs.random_case(6000 + m + 7 * n + 13 * k, m, n, k, kind="normal"),
+                      f"bf16 skinny normal {shape}")
