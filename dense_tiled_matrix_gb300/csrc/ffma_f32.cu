@@ -198,6 +198,10 @@ ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     extern __shared__ uint8_t smem_raw[];
     const Smem sm(smem_raw);
     const int warp_all = threadIdx.x >> 5;
+    // The next launch of a split product (pieces after whole tiles, the reduce
+    // after the pieces) may start on SMs this grid frees; it reads nothing this
+    // grid writes (the reduce waits for the pieces on the device).
+    griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     // Tile origin and k-range of this block (recomputed where needed rather
     // than held in registers through the consumers' loop).
@@ -288,6 +292,10 @@ ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 #pragma unroll
         for (int p = 0; p < 4; p += 2)
             dst[(i * 2 + p / 2) * F::THREADS] = make_float4(acc[i][p].x, acc[i][p].y, acc[i][p + 1].x, acc[i][p + 1].y);
+    // Launched as a dependent of the whole-tile grid, the pieces may finish
+    // first; waiting for that grid here makes this grid's completion (which
+    // the reduce waits for) imply that every tile of C has been written.
+    griddep_wait();
 }
 
 // C of the remainder tiles: tile tile0 + b is the sum of the pieces in
@@ -304,6 +312,7 @@ ffma_f32_reduce_kernel(const float* __restrict__ ws, float* __restrict__ C, int6
     const int b_col0 = 64 * wn + 4 * tn;
     int tile_m, tile_n;
     tile_coords(tile0 + blockIdx.x, (M + kBM - 1) / kBM, (N + kBN - 1) / kBN, tile_m, tile_n);
+    griddep_wait();   // the pieces have been written (launched as their dependent)
     Acc acc;
     zero(acc);
     const float4* src = reinterpret_cast<const float4*>(ws + static_cast<int64_t>(blockIdx.x) * parts * kBM * kBN) + tid;
@@ -324,18 +333,39 @@ ffma_f32_reduce_kernel(const float* __restrict__ ws, float* __restrict__ C, int6
 }
 
 // The warp-specialised 128-row kernel over `grid` blocks (see its comment).
+// Launch configuration on p.stream; with `dependent`, as a programmatic
+// dependent of the kernel before it (it may start while that one finishes).
+cudaLaunchConfig_t launch_config(const Problem& p, unsigned grid, unsigned threads, size_t smem, bool dependent,
+                                 cudaLaunchAttribute* attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = p.stream;
+    if (dependent) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cfg;
+}
+
 cudaError_t launch_ws(const Problem& p, const CUtensorMap& ta, const CUtensorMap& tb, int64_t grid, int64_t tile0,
-                      int parts, float* ws, int vec_store, const Device& dev) {
+                      int parts, float* ws, int vec_store, const Device& dev, bool dependent) {
     cudaError_t err = cudaFuncSetAttribute(ffma_f32_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(FCfg::SMEM));
     if (err != cudaSuccess) {
         set_error("cudaFuncSetAttribute(ffma_f32_ws_kernel): %s", cudaGetErrorString(err));
         return err;
     }
-    ffma_f32_ws_kernel<<<static_cast<unsigned>(grid), kWsThreads, FCfg::SMEM, p.stream>>>(
-        ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status, static_cast<int>(tile0), parts, ws);
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg =
+        launch_config(p, static_cast<unsigned>(grid), kWsThreads, FCfg::SMEM, dependent, attr);
+    err = cudaLaunchKernelEx(&cfg, ffma_f32_ws_kernel, ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status,
+                             static_cast<int>(tile0), parts, ws);
     count_launch();
-    return cudaSuccess;
+    return err;
 }
 
 bool make_maps(const Problem& p, CUtensorMap* ta, CUtensorMap* tb) {
@@ -386,7 +416,7 @@ cudaError_t launch_tiles(const Problem& p, const Device& dev) {
     CUtensorMap ta, tb;
     if (!make_maps(p, &ta, &tb)) return cudaErrorInvalidValue;
     const int64_t tiles = static_cast<int64_t>((p.m + F::BM - 1) / F::BM) * ((p.n + kBN - 1) / kBN);
-    cudaError_t err = launch_ws(p, ta, tb, tiles, 0, 1, nullptr, vec_store_ok(p), dev);
+    cudaError_t err = launch_ws(p, ta, tb, tiles, 0, 1, nullptr, vec_store_ok(p), dev, false);
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) set_error("ffma_f32_ws_kernel launch: %s", cudaGetErrorString(err));
     return err;
@@ -403,13 +433,23 @@ cudaError_t launch_split_tail(const Problem& p, const Device& dev, void* workspa
     const int vec_store = vec_store_ok(p);
     float* ws = static_cast<float*>(workspace);
     cudaError_t err = cudaSuccess;
-    if (st.full > 0) err = launch_ws(p, ta, tb, st.full, 0, 1, nullptr, vec_store, dev);
-    if (err == cudaSuccess) err = launch_ws(p, ta, tb, st.rest * st.parts, st.full, st.parts, ws, vec_store, dev);
-    if (err != cudaSuccess) return err;
-    ffma_f32_reduce_kernel<<<static_cast<unsigned>(st.rest), F::THREADS, 0, p.stream>>>(
-        ws, p.C, p.ldc, p.m, p.n, static_cast<int>(st.full), st.parts, vec_store);
+    // Whole tiles first (an ordinary launch: everything before it in the
+    // stream has completed), then the pieces of the remainder, which read only
+    // A and B and so start as soon as the whole-tile grid frees SMs, then the
+    // reduce, which waits on the device for the pieces.
+    if (st.full > 0) err = launch_ws(p, ta, tb, st.full, 0, 1, nullptr, vec_store, dev, false);
+    if (err == cudaSuccess)
+        err = launch_ws(p, ta, tb, st.rest * st.parts, st.full, st.parts, ws, vec_store, dev, st.full > 0);
+    if (err != cudaSuccess) {
+        set_error("ffma_f32_ws_kernel launch: %s", cudaGetErrorString(err));
+        return err;
+    }
+    cudaLaunchAttribute attr[1];
+    const cudaLaunchConfig_t cfg = launch_config(p, static_cast<unsigned>(st.rest), F::THREADS, 0, true, attr);
+    err = cudaLaunchKernelEx(&cfg, ffma_f32_reduce_kernel, static_cast<const float*>(ws), p.C, p.ldc, p.m, p.n,
+                             static_cast<int>(st.full), st.parts, vec_store);
     count_launch();
-    err = cudaGetLastError();
+    if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) set_error("ffma_f32 split launches: %s", cudaGetErrorString(err));
     return err;
 }
