@@ -11,7 +11,10 @@ passes ("wavefronts") of a warp-wide access is the largest number of
 distinct words any bank must deliver.
 
 The FFMA kernel's addressing is restated here from its source and checked to
-need one pass per instruction; the TMA 64-byte swizzle it relies on is
+need one pass per instruction, i.e. to have no bank conflict (the hardware's
+own count for a 128-bit load, ncu's wavefronts, is at least 2 -- 2 for the A
+reads, 4 for the B reads on GB300 -- and bank conflicts would add to it); the
+TMA 64-byte swizzle it relies on is
 checked against the kernel's own chunk formula.  So are the TMA transpose's
 reads of a 128-byte-swizzled input tile and its writes of the output tile.
 """
