@@ -258,3 +258,17 @@ def test_skinny_bf16_row_forms(shape):
                       f"bf16 skinny int {shape}")
     parity.full_check("bf16", inputs.random_case(6000 + m + 7 * n + 13 * k, m, n, k, kind="normal"),
                       f"bf16 skinny normal {shape}")
+
+
+# One very large extent at a time (the other two small): grid and tile
+# indices far beyond the other tests, TMA coordinates into the millions, and
+# the skinny kernel with 65536 column tiles.  Checked element by element.
+LARGE_EXTENT_SHAPES = [(1, 8388608, 16), (1048576, 8, 32), (3000, 3, 20000), (64, 2097152, 16)]
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", LARGE_EXTENT_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_large_single_extent(mode, shape):
+    m, n, k = shape
+    parity.full_check(mode, inputs.random_case(7000 + m % 997 + 7 * (n % 991) + 13 * k, m, n, k, kind="int"),
+                      f"{mode} int {shape}")
