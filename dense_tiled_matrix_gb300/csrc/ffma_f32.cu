@@ -62,16 +62,18 @@ constexpr int kStages = 8;               // 4 -> 8: 57.8 -> 59.0 TFLOP/s at 4096
 constexpr int kTR = 8;                   // rows of C per consumer thread (8 or 16)
 constexpr int kRowGroup = 8;             // rows of a thread processed together (4 or 8)
 constexpr int kChunkUnroll = 4;          // unrolling of the 4-wide k chunks of a stage (1..4)
+constexpr int kWarpsM = 4;               // consumer warps along M (two along N); 6 (192-row tiles,
+                                         // 160 registers a consumer) measured 4 % slower at 4096^3
 constexpr int kGroupM = 8;
 constexpr uint32_t kStageB = kBK * kBN * 4;   // 8 KiB
 
-// Eight consumer warps, four along M and two along N, each warp 4 kTR rows x
-// 64 columns: kTR = 8 gives 128 x 128 tiles.  (A 64-row form, two CTAs per
+// kWarpsM x 2 consumer warps, each warp 4 kTR rows x 64 columns: kWarpsM = 4
+// and kTR = 8 give eight warps and 128 x 128 tiles.  (A 64-row form, two CTAs per
 // SM, served k < 2048 until the warp-specialised 128-row kernel beat it
 // there too: 4096 x 4096 x 1024 50.9 -> 55.6 TFLOP/s.)
 struct FCfg {
-    static constexpr int BM = 16 * kTR;
-    static constexpr int THREADS = 256;
+    static constexpr int BM = 4 * kTR * kWarpsM;
+    static constexpr int THREADS = 64 * kWarpsM;
     static constexpr int WARPS = THREADS / 32;
     static constexpr uint32_t STAGE_A = BM * kBK * 4;   // 8 KiB at 128 rows
     static constexpr size_t SMEM = 1024 + kStages * (STAGE_A + kStageB) + 2 * kStages * sizeof(uint64_t);
@@ -190,9 +192,12 @@ struct Smem {
 // u % parts (k-phases [KT p / parts, KT (p + 1) / parts)) of tile
 // tile0 + u / parts, whose partial sums go to slot u of `ws` (float4 j of
 // consumer thread t at j * 256 + t) for ffma_f32_reduce_kernel.
-constexpr int kWsThreads = 384;
-constexpr int kProducerRegs = 24, kConsumerRegs = 240;
-static_assert(128 * kProducerRegs + 256 * kConsumerRegs <= 65536, "register split exceeds the file");
+constexpr int kWsThreads = 128 + FCfg::THREADS;
+constexpr int kProducerRegs = 24;
+constexpr int kConsumerRegs = (65536 - 128 * kProducerRegs) / FCfg::THREADS / 8 * 8 > 240
+                                  ? 240
+                                  : (65536 - 128 * kProducerRegs) / FCfg::THREADS / 8 * 8;
+static_assert(128 * kProducerRegs + FCfg::THREADS * kConsumerRegs <= 65536, "register split exceeds the file");
 
 __global__ void __launch_bounds__(kWsThreads, 1)
 ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
