@@ -17,7 +17,11 @@ The same JSON line carries, for information, the other measured shapes
 4097 x 3001 x 1023 fp32 edge-tile case), a roofline object for the kernel
 taking most of the step's time, the end-to-end number through the C ABI from
 pinned host buffers, the CPU oracle timed on a bounded sample of the same
-workload, and the SM clocks sampled while timing.
+workload, and the SM clocks sampled while timing.  After the timed region each
+shape is also launched back to back between a single event pair
+(``ms_back_to_back``): the per-launch event pairs add a microsecond or two,
+which shows on the 16 x 8192 x 8192 case (~28 us); ``ms`` and the roofline
+keep the per-launch figure.
 
 ``--impl reference`` times the CPU oracle instead (a bounded sample of the
 same workload per step) and prints the same metric for it.
@@ -315,6 +319,23 @@ def bench_tgemm(args, world, rank, local):
         torch.cuda.synchronize(dev)
         return {n: [a.elapsed_time(b) / 1e3 for a, b in v] for n, v in times.items()}
 
+    def back_to_back(runs, iters):
+        """Mean device time (s) of `iters` launches issued back to back between one event pair
+        (no events in between; copies rotated as above).  Reported beside the per-launch figure:
+        an event pair around every launch adds its own ~1-2 us, which matters for short kernels."""
+        out = {}
+        for name, (c, copies, C, fn) in runs.items():
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for it in range(iters):
+                A, B = copies[it % len(copies)]
+                fn(A, B, C, stream)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            out[name] = e0.elapsed_time(e1) / 1e3 / iters
+        return out
+
     runs = {name: prepare(spec) for name, spec in PARTS.items()}
     extras = {} if args.no_extras else {name: prepare(spec) for name, spec in EXTRAS.items()}
 
@@ -331,6 +352,9 @@ def bench_tgemm(args, world, rank, local):
         barrier(world)
         slow = {n: args.warmup + SLOW_EXTRA_ITERS for n in extras if n.startswith("pages")}
         extra_times = timed(extras, args.warmup + args.steps, iters_of=slow) if extras else {}
+        # after the timed region: the same launches back to back (not the pages' slow kernels)
+        b2b = back_to_back(runs, args.steps)
+        b2b.update(back_to_back({n: r for n, r in extras.items() if n not in slow}, args.steps))
     step_s = sum(sum(v) for v in per.values()) / args.steps
     step_s = max_over_ranks(step_s, world)
     flops_step = sum(2.0 * runs[n][0].m * runs[n][0].n * runs[n][0].k for n in runs)
@@ -349,6 +373,10 @@ def bench_tgemm(args, world, rank, local):
                        "ms": round(avg * 1e3, 4),
                        "tflops": round(2.0 * c.m * c.n * c.k / avg / 1e12, 2),
                        "roofline": roof_part}
+        if name in b2b:
+            # informational: `ms`, `tflops` and the roofline use the per-launch event pairs
+            parts[name]["ms_back_to_back"] = round(b2b[name] * 1e3, 4)
+            parts[name]["roofline_frac_back_to_back"] = round(roof_part["frac"] * avg / b2b[name], 4)
     dominant = max(PARTS, key=lambda n: sum(per[n]))
     roof = dict(parts[dominant]["roofline"])
     roof["kernel"] = KERNEL_NAMES[PARTS[dominant][1]]
