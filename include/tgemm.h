@@ -22,8 +22,8 @@
  * library may take temporary stream-ordered workspace on `stream` (for
  * operands whose base address or leading dimension is not a multiple of 16
  * bytes, for B transposed on the TF32 path, and for the partial sums of
- * tiles that tgemm_f32 splits between two blocks) and returns it on the same
- * stream.
+ * tiles that tgemm_f32 splits along k between several blocks) and returns it
+ * on the same stream.
  *
  * Execution.  Every call is asynchronous on `stream` (NULL is the legacy
  * default stream) and returns once the work is queued.  Argument errors are
@@ -31,7 +31,11 @@
  * TGEMM_ERR_CUDA.  Faults during execution surface at the caller's next
  * synchronisation; a kernel whose internal pipeline wait exceeds its time
  * limit stops, records TGEMM_ERR_TIMEOUT in a per-device status word and
- * exits, and tgemm_get_device_status() reports it.
+ * exits, and tgemm_get_device_status() reports it.  Some kernels are
+ * launched as programmatic dependents of the kernel queued before them: they
+ * may start early, but wait on the device for that kernel to complete before
+ * they touch global memory, and a call's last kernel completes only after
+ * all of the call's work, so stream order holds for every buffer.
  *
  * Results.  tgemm_f32 multiplies in fp32 with fused multiply-add (one
  * rounding per term); tgemm_tf32 feeds fp32 inputs to the tensor cores as
