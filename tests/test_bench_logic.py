@@ -1,0 +1,68 @@
+"""bench.py's host-side arithmetic, on the CPU: the roofline object of each path
+and the parsing of the nvidia-smi clock log (no GPU, no subprocess)."""
+import os
+from collections import namedtuple
+
+import pytest
+
+import bench
+
+Case = namedtuple("Case", "m n k")
+PEAKS = {"hbm_gbs": 6792.0, "bf16_tflops": 1904.1}
+
+
+def test_skinny_bf16_is_hbm_bound_on_algorithmic_bytes():
+    c = Case(16, 8192, 8192)
+    r = bench.roofline_for("bf16", c, 28.0e-6, PEAKS, "measured")
+    nbytes = 2 * (16 * 8192 + 8192 * 8192) + 4 * 16 * 8192   # A and B read once (bf16), C written once (fp32)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["algorithmic_bytes"] == nbytes
+    assert r["achieved"] == pytest.approx(nbytes / 28.0e-6 / 1e9, abs=0.05)
+    assert r["frac"] == pytest.approx(r["achieved"] / 6792.0, abs=1e-4)
+
+
+@pytest.mark.parametrize("entry, bound, peak", [
+    ("f32", "alu", 152 * 128 * 2 * 2070e6 / 1e12),
+    ("pages_naive", "alu", 152 * 128 * 2 * 2070e6 / 1e12),
+    ("bf16", "tensor", 1904.1),
+    ("tf32", "tensor", 1904.1 * 1100.0 / 2250.0),
+])
+def test_compute_bound_paths_use_their_own_peak(entry, bound, peak):
+    c = Case(4096, 4096, 4096)
+    r = bench.roofline_for(entry, c, 2.0e-3, PEAKS, "measured")
+    flops = 2.0 * 4096 ** 3
+    assert r["bound"] == bound and r["unit"] == "TFLOP/s" and r["algorithmic_flops"] == int(flops)
+    assert r["peak"] == pytest.approx(peak, abs=0.01)
+    assert r["achieved"] == pytest.approx(flops / 2.0e-3 / 1e12, abs=0.01)
+    assert r["frac"] == pytest.approx(flops / 2.0e-3 / 1e12 / peak, abs=1e-4)
+
+
+def _summary(tmp_path, lines):
+    s = bench.ClockSampler(0)
+    s.path = os.path.join(tmp_path, "clocks.csv")
+    with open(s.path, "w") as fh:
+        fh.write("\n".join(lines) + "\n")
+    s.proc = object()   # as if nvidia-smi had run
+    return s.summary()
+
+
+def test_clock_log_median_and_no_reasons(tmp_path):
+    rows = [f"0, {mhz}, 2070, 450.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active"
+            for mhz in (2070, 2055, 2070, 1980, 2070)]
+    out = _summary(tmp_path, rows)
+    assert out["sm_mhz"] == 2070 and out["sm_max_mhz"] == 2070 and out["reasons"] == []
+    assert out["samples"] == 5 and out["power_w_max"] == 450.5
+
+
+def test_clock_log_reports_every_throttle_reason_seen(tmp_path):
+    rows = ["0, 2070, 2070, 900.0, 0x4, Not Active, Not Active, Not Active, Active",
+            "0, 1800, 2070, 1300.0, 0x48, Not Active, Active, Not Active, Active",
+            "0, 2070, 2070, 800.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+            "garbled line"]
+    out = _summary(tmp_path, rows)
+    assert out["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert out["samples"] == 3 and out["sm_mhz"] == 2070
+
+
+def test_clock_log_without_samples(tmp_path):
+    out = _summary(tmp_path, [""])
+    assert out["reasons"] == ["no samples"] and out["sm_mhz"] is None
