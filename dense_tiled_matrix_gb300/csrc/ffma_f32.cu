@@ -128,12 +128,12 @@ __device__ __forceinline__ void fma_phase(Acc& acc, const float* As, const float
                 const float2 bp[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w),
                                       make_float2(b1.x, b1.y), make_float2(b1.z, b1.w)};
 #pragma unroll
-                for (int ii = 0; ii < kRowGroup; ++ii) {
-                    const float a = kk == 0 ? av[ii].x : kk == 1 ? av[ii].y : kk == 2 ? av[ii].z : av[ii].w;
-                    const float2 aa = make_float2(a, a);
+                for (int p = 0; p < 4; ++p) {
 #pragma unroll
-                    for (int p = 0; p < 4; ++p)
-                        acc[kRowGroup * g + ii][p] = __ffma2_rn(aa, bp[p], acc[kRowGroup * g + ii][p]);
+                    for (int ii = 0; ii < kRowGroup; ++ii) {
+                        const float a = kk == 0 ? av[ii].x : kk == 1 ? av[ii].y : kk == 2 ? av[ii].z : av[ii].w;
+                        acc[kRowGroup * g + ii][p] = __ffma2_rn(make_float2(a, a), bp[p], acc[kRowGroup * g + ii][p]);
+                    }
                 }
             }
         }
