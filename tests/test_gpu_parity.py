@@ -185,7 +185,7 @@ def test_tf32_input_conversion(capsys):
 def _boundary_shapes(count, seed, budget=1.2e9):
     """Seeded shapes that sit near the dispatch boundaries: m around 64 (the
     skinny bf16 kernel), sizes around multiples of 64/128/224/256 (tile edges),
-    k around 2048 and 3072 (fp32 tile height, tensor-core tile height) and
+    k around 2048 and 3072 (the tensor-core tile height switches at 3072) and
     tile counts around multiples of 152 (a partly empty last wave: split
     pieces, 224-wide tiles, stream-K)."""
     rng = np.random.default_rng(seed)
