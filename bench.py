@@ -26,19 +26,35 @@ keep the per-launch figure.
 ``--impl reference`` times the CPU oracle instead (a bounded sample of the
 same workload per step) and prints the same metric for it.
 
+Per shape, ``ms`` is the median of the per-launch event timings (the mean is
+reported beside it).  The FP32 FMA peak is derived at run time from the SM
+count the device reports and the highest SM clock nvidia-smi reported while
+timing; tensor-core fractions are given against the measured peaks of
+MEASURED_PEAKS.json (``frac``) and against the nominal dense peaks
+(``frac_of_nominal``).  DRAM traffic per call comes from the ncu table
+profiles/dram_traffic.csv and is reported as null once the kernel sources it
+was captured on have changed.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tgemm|reference]
-Under torchrun each rank runs its own copy of the step (weak scaling, no
-collective on the data path); rank 0 prints the line.
+                       [--shard rows|replicas]
+Under torchrun (N > 1) the step's two products are split by rows across the
+ranks by default (``--shard rows``: rank r computes its row block of each C
+from the same rows of A and all of B, one independent call per product on its
+own GPU, no collective on the data path; strong scaling, ``value`` = the full
+products' flops / the slowest rank's step time).  ``--shard replicas`` runs
+the whole step on every rank instead (weak scaling).  Rank 0 prints the line.
 """
 from __future__ import annotations
 
 import argparse
+import csv
+import hashlib
 import json
-import math
 import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -47,10 +63,10 @@ if ROOT not in sys.path:
 
 METRIC = "GEMM TFLOPS (2mnk/s) at 4096³ fp32 & 8192³ bf16; % of GB300 roofline"
 UNIT = "TFLOP/s"
-SM_COUNT = 152
-SM_MAX_MHZ = 2070.0
-FFMA_PEAK_TFLOPS = SM_COUNT * 128 * 2 * SM_MAX_MHZ * 1e6 / 1e12   # 80.54
-NOMINAL_BF16, NOMINAL_TF32 = 2250.0, 1100.0
+FP32_LANES_PER_SM = 128          # FP32 FMA lanes per SM (sm_100 family)
+NOMINAL_BF16, NOMINAL_TF32 = 2250.0, 1100.0   # dense tensor peaks, TFLOP/s
+CSRC = os.path.join(ROOT, "dense_tiled_matrix_gb300", "csrc")
+TRAFFIC_TABLE = os.path.join(ROOT, "profiles", "dram_traffic.csv")
 
 # name -> (workload, entry, dtype)
 PARTS = {
@@ -61,21 +77,56 @@ EXTRAS = {
     "tf32_4096": ("n4096", "tf32", "f32"),
     "skinny_bf16": ("skinny", "bf16", "bf16"),
     "irregular_f32": ("irregular", "f32", "f32"),
-    # the pages' own kernels (libtgemm_pages), for the naive -> tiled comparison
+    "irregular_tf32": ("irregular", "tf32", "f32"),
+    "irregular_bf16": ("irregular", "bf16", "bf16"),
+    # the pages' own experiment (naive -> tiled -> libtgemm) at 1024^3 and 4096^3
+    "f32_1024": ("int1024", "f32", "f32"),
+    "pages_naive_1024": ("int1024", "pages_naive", "f32"),
+    "pages_tiled16_1024": ("int1024", "pages_tiled16", "f32"),
+    "pages_tiled32_1024": ("int1024", "pages_tiled32", "f32"),
     "pages_naive_4096": ("n4096", "pages_naive", "f32"),
     "pages_tiled16_4096": ("n4096", "pages_tiled16", "f32"),
     "pages_tiled32_4096": ("n4096", "pages_tiled32", "f32"),
 }
-SLOW_EXTRA_ITERS = 4   # timed launches of the pages' kernels (tens of ms each)
-# DRAM bytes (read + write) per launch of the main kernel of a shape, from one
-# ncu capture of the current kernel (summaries under profiles/).  Must be
-# re-taken whenever that kernel changes; shapes without an entry report null.
-NCU_TRAFFIC = {
-    "f32_4096": (431.77e6, "profiles/ffma_f32_4096.md (the three launches of one tgemm_f32 call)"),
-    "bf16_8192": (1112.98e6, "profiles/umma_bf16_8192.md (umma_kernel<0, 0, 1, 256, 0>)"),
-    "tf32_4096": (237.49e6, "profiles/umma_tf32_4096.md (umma_kernel<1, 1, 1, 224, 0>, without the B transpose)"),
-}
+SLOW_EXTRAS = {"pages_naive_4096", "pages_tiled16_4096", "pages_tiled32_4096"}
+SLOW_EXTRA_ITERS = 4   # timed launches of the pages' kernels at 4096^3 (tens of ms each)
 KERNEL_NAMES = {"f32": "ffma_f32_ws_kernel (912 tiles, then 448 split pieces) + ffma_f32_reduce_kernel (one tgemm_f32 call)", "tf32": "umma_kernel<1, 1, 1, 224, 0>", "bf16": "umma_kernel<0, 0, 1, 256, 0>"}
+
+
+def source_digest(files):
+    """First 16 hex digits of the sha256 of the named csrc files, concatenated in order."""
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_table(path=TRAFFIC_TABLE):
+    """part -> {"bytes": int or None, "source": str, "stale": bool} from the ncu traffic table.
+    An entry whose kernel sources have changed since the capture gives bytes None."""
+    out = {}
+    try:
+        with open(path, newline="") as fh:
+            rows = [line for line in fh if not line.startswith("#")]
+    except OSError:
+        return out
+    for row in csv.DictReader(rows):
+        files = row["sources"].split()
+        try:
+            current = source_digest(files)
+        except OSError:
+            current = None
+        stale = current != row["sha256_16"]
+        out[row["part"]] = {"bytes": None if stale else int(row["bytes_per_call"]),
+                            "source": f"{row['summary']} ({row['kernels']})", "stale": stale}
+    return out
+
+
+def fp32_peak(sm_count, sm_max_mhz):
+    """(TFLOP/s, derivation) of the FP32 FMA peak: SMs x lanes x 2 flop x max SM clock."""
+    tf = sm_count * FP32_LANES_PER_SM * 2 * sm_max_mhz * 1e6 / 1e12
+    return tf, f"{sm_count} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 flop x {sm_max_mhz:.0f} MHz = {tf:.2f} TFLOP/s"
 
 
 def load_peaks():
@@ -88,31 +139,37 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def roofline_for(entry, case, seconds, peaks, peaks_src):
-    """Roofline object of one launch: skinny bf16 is HBM-bound, the rest compute-bound."""
+def roofline_for(entry, case, seconds, peaks, peaks_src, fp32=None):
+    """Roofline object of one launch: skinny bf16 is HBM-bound, the rest compute-bound.
+    ``fp32`` = (peak TFLOP/s, derivation) of the FP32 FMA pipes (fp32_peak)."""
     flops = 2.0 * case.m * case.n * case.k
     es = 2 if entry == "bf16" else 4
     bytes_ = es * (case.m * case.k + case.k * case.n) + 4 * case.m * case.n
-    if case.m <= 64:
+    if entry == "bf16" and case.m <= 64:
         achieved = bytes_ / seconds / 1e9
         peak = float(peaks["hbm_gbs"])
         return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": None,
                 "peak_source": f"hbm_gbs of {peaks_src}", "algorithmic_bytes": int(bytes_)}
     achieved = flops / seconds / 1e12
+    nominal = None
     if entry == "f32" or entry.startswith("pages"):
-        peak, src = FFMA_PEAK_TFLOPS, "152 SMs x 128 FP32 lanes x 2 x 2070 MHz"
+        peak, src = fp32 if fp32 is not None else fp32_peak(152, 2070.0)
         bound = "alu"
     elif entry == "bf16":
-        peak, src = float(peaks["bf16_tflops"]), f"bf16_tflops (burst) of {peaks_src}"
-        bound = "tensor"
+        peak, src = float(peaks["bf16_tflops"]), f"bf16_tflops (burst, cuBLAS) of {peaks_src}"
+        bound, nominal = "tensor", NOMINAL_BF16
     else:
         peak = float(peaks["bf16_tflops"]) * NOMINAL_TF32 / NOMINAL_BF16
-        src = f"bf16_tflops (burst) of {peaks_src} x 1.1/2.25 (nominal tf32/bf16)"
-        bound = "tensor"
-    return {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": "TFLOP/s",
-            "frac": round(achieved / peak, 4), "traffic": None, "peak_source": src,
-            "algorithmic_flops": int(flops)}
+        src = f"bf16_tflops (burst, cuBLAS) of {peaks_src} x 1.1/2.25 (nominal tf32/bf16)"
+        bound, nominal = "tensor", NOMINAL_TF32
+    out = {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 2), "unit": "TFLOP/s",
+           "frac": round(achieved / peak, 4), "traffic": None, "peak_source": src,
+           "algorithmic_flops": int(flops)}
+    if nominal is not None:
+        out["nominal_peak"] = nominal
+        out["frac_of_nominal"] = round(achieved / nominal, 4)
+    return out
 
 
 class ClockSampler:
@@ -125,12 +182,12 @@ class ClockSampler:
     def __init__(self, device_index):
         self.device_index = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.path = None
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.fh = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(prefix=f"tgemm_clocks_{os.getpid()}_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.device_index}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
@@ -140,6 +197,8 @@ class ClockSampler:
                 time.sleep(0.05)
         except OSError:
             self.proc = None
+            if getattr(self, "fh", None) is not None:
+                self.fh.close()
         return self
 
     def __exit__(self, *exc):
@@ -160,6 +219,10 @@ class ClockSampler:
                 parts = [p.strip() for p in line.split(",")]
                 if len(parts) >= 9:
                     rows.append(parts)
+        try:
+            os.unlink(self.path)   # the log is only read here
+        except OSError:
+            pass
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
         sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
@@ -175,6 +238,17 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows),
                 "window": "warm-up, timed steps and extra shapes (nvidia-smi every 100 ms)",
                 "power_w_max": max(power) if power else None}
+
+
+def step_config(world, shard_rows):
+    """The ``config`` object of the JSON line (the same for both arms)."""
+    if shard_rows:
+        parallelism = f"rows x{world} (each rank its row block of every product; no collective)"
+    else:
+        parallelism = f"replicas x{world}"
+    return {"workload": "gemm 8192x8192x8192 bf16->fp32 (tcgen05) + 4096x4096x4096 fp32 (FFMA)",
+            "l2": "inputs larger than L2: each launch reads the next of R input copies (>= 384 MiB per shape)",
+            "parallelism": parallelism}
 
 
 def dist_setup(args):
@@ -252,10 +326,11 @@ def bench_reference(args, world, rank):
               f"(fp64 oracle, {cores} threads)")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total / len(per_step) * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded SplitMix64)",
+            "scaling": "strong" if world > 1 and args.shard == "rows" else "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded SplitMix64)",
             "impl": "reference",
-            "config": {"workload": "gemm 8192x8192x8192 bf16->fp32 + 4096x4096x4096 fp32 (oracle row sample)",
-                       "rows_per_part": rows, "l2": "n/a (CPU)"},
+            "config": step_config(world, world > 1 and args.shard == "rows"),
+            "reference_sample": {"rows_per_part": rows, "l2": "n/a (CPU)"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -264,14 +339,17 @@ def bench_reference(args, world, rank):
 def bench_tgemm(args, world, rank, local):
     import torch
 
-    from dense_tiled_matrix_gb300 import inputs, pages, tgemm
+    from dense_tiled_matrix_gb300 import inputs, pages, sharding, tgemm
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     tgemm.load()
     peaks, peaks_src = load_peaks()
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     stream = torch.cuda.current_stream(dev)
     rotate_bytes = 384 * 2 ** 20
+    # Row sharding (N > 1, default): this rank's rows of every product of the step.
+    shard_rows = world > 1 and args.shard == "rows"
 
     def to_dev(arr):
         import numpy as np
@@ -286,20 +364,28 @@ def bench_tgemm(args, world, rank, local):
             case_cache[name] = inputs.make(name)
         return case_cache[name]
 
-    def prepare(spec):
+    class Shape:
+        def __init__(self, m, n, k):
+            self.m, self.n, self.k = m, n, k
+
+    def prepare(spec, shard):
         wl, entry, _ = spec
         c = case_of(wl)
         cc = inputs.convert(c, "bf16" if entry == "bf16" else "f32")
-        A0, B0 = to_dev(cc.A), to_dev(cc.B)
+        A_host = cc.A
+        if shard:
+            r0, r1 = sharding.rows(c.m, world, rank)
+            A_host = A_host[r0:r1]
+        A0, B0 = to_dev(A_host), to_dev(cc.B)
         per_copy = A0.numel() * A0.element_size() + B0.numel() * B0.element_size()
         R = max(1, -(-rotate_bytes // per_copy))
         copies = [(A0, B0)] + [(A0.clone(), B0.clone()) for _ in range(R - 1)]
-        C = torch.empty((c.m, c.n), dtype=torch.float32, device=dev)
+        C = torch.empty((A0.shape[0], c.n), dtype=torch.float32, device=dev)
         fn = {"f32": tgemm.tgemm_f32, "tf32": tgemm.tgemm_tf32, "bf16": tgemm.tgemm_bf16,
               "pages_naive": lambda A, B, C, st: pages.tgemm_pages_naive_f32(A, B, C, st),
               "pages_tiled16": lambda A, B, C, st: pages.tgemm_pages_tiled_f32(A, B, C, 16, st),
               "pages_tiled32": lambda A, B, C, st: pages.tgemm_pages_tiled_f32(A, B, C, 32, st)}[entry]
-        return c, copies, C, fn
+        return Shape(A0.shape[0], c.n, c.k), copies, C, fn
 
     def timed(runs, iters, start=0, iters_of=None):
         """Per-launch device times (s) of `iters` launches of each of `runs`; launch i reads copy i mod R."""
@@ -336,8 +422,8 @@ def bench_tgemm(args, world, rank, local):
             out[name] = e0.elapsed_time(e1) / 1e3 / iters
         return out
 
-    runs = {name: prepare(spec) for name, spec in PARTS.items()}
-    extras = {} if args.no_extras else {name: prepare(spec) for name, spec in EXTRAS.items()}
+    runs = {name: prepare(spec, shard_rows) for name, spec in PARTS.items()}
+    extras = {} if args.no_extras or rank != 0 else {name: prepare(spec, False) for name, spec in EXTRAS.items()}
 
     with ClockSampler(local) as clocks:
         timed(runs, args.warmup)
@@ -350,33 +436,45 @@ def bench_tgemm(args, world, rank, local):
         t_wall = time.perf_counter() - t_wall0
         launches = tgemm.tgemm_kernel_launches() - launches0
         barrier(world)
-        slow = {n: args.warmup + SLOW_EXTRA_ITERS for n in extras if n.startswith("pages")}
+        slow = {n: args.warmup + SLOW_EXTRA_ITERS for n in extras if n in SLOW_EXTRAS}
         extra_times = timed(extras, args.warmup + args.steps, iters_of=slow) if extras else {}
         # after the timed region: the same launches back to back (not the pages' slow kernels)
         b2b = back_to_back(runs, args.steps)
         b2b.update(back_to_back({n: r for n, r in extras.items() if n not in slow}, args.steps))
+    clock_summary = clocks.summary()
     step_s = sum(sum(v) for v in per.values()) / args.steps
     step_s = max_over_ranks(step_s, world)
-    flops_step = sum(2.0 * runs[n][0].m * runs[n][0].n * runs[n][0].k for n in runs)
-    value = world * flops_step / step_s / 1e12
+    if shard_rows:
+        # the full products' flops: the ranks' row blocks together cover every row once
+        flops_step = sum(2.0 * case_of(PARTS[n][0]).m * runs[n][0].n * runs[n][0].k for n in runs)
+        value = flops_step / step_s / 1e12
+    else:
+        flops_step = sum(2.0 * runs[n][0].m * runs[n][0].n * runs[n][0].k for n in runs)
+        value = world * flops_step / step_s / 1e12
+
+    # FP32 peak from the device's SM count and the highest SM clock seen while timing
+    max_mhz = clock_summary.get("sm_max_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+    fp32 = fp32_peak(sm_count, float(max_mhz))
+    traffic = traffic_table()
 
     parts = {}
     for name, ts in list(per.items()) + [(n, v[args.warmup:]) for n, v in extra_times.items()]:
         c = (runs.get(name) or extras.get(name))[0]
         entry = (PARTS.get(name) or EXTRAS.get(name))[1]
-        avg = sum(ts) / len(ts)
-        roof_part = roofline_for(entry, c, avg, peaks, peaks_src)
-        if name in NCU_TRAFFIC:
-            roof_part["traffic"] = int(NCU_TRAFFIC[name][0])
-            roof_part["traffic_source"] = NCU_TRAFFIC[name][1]
+        med = statistics.median(ts)
+        roof_part = roofline_for(entry, c, med, peaks, peaks_src, fp32)
+        if name in traffic:
+            roof_part["traffic"] = traffic[name]["bytes"]
+            roof_part["traffic_source"] = traffic[name]["source"] + (" -- stale: kernel changed since the capture"
+                                                                     if traffic[name]["stale"] else "")
         parts[name] = {"m": c.m, "n": c.n, "k": c.k, "entry": f"tgemm_{entry}", "launches_timed": len(ts),
-                       "ms": round(avg * 1e3, 4),
-                       "tflops": round(2.0 * c.m * c.n * c.k / avg / 1e12, 2),
+                       "ms": round(med * 1e3, 4), "ms_mean": round(sum(ts) / len(ts) * 1e3, 4),
+                       "tflops": round(2.0 * c.m * c.n * c.k / med / 1e12, 2),
                        "roofline": roof_part}
         if name in b2b:
             # informational: `ms`, `tflops` and the roofline use the per-launch event pairs
             parts[name]["ms_back_to_back"] = round(b2b[name] * 1e3, 4)
-            parts[name]["roofline_frac_back_to_back"] = round(roof_part["frac"] * avg / b2b[name], 4)
+            parts[name]["roofline_frac_back_to_back"] = round(roof_part["frac"] * med / b2b[name], 4)
     dominant = max(PARTS, key=lambda n: sum(per[n]))
     roof = dict(parts[dominant]["roofline"])
     roof["kernel"] = KERNEL_NAMES[PARTS[dominant][1]]
@@ -386,7 +484,7 @@ def bench_tgemm(args, world, rank, local):
     # padded tile) next to libtgemm's transpose, at the lecture's 1024 x 1024
     # and at 16384 x 16384 (HBM-bound); GB/s counts the bytes read and written.
     transposes = {}
-    if not args.no_extras:
+    if extras:
         gen = torch.Generator(device=dev)
         gen.manual_seed(1006)
         kernels = {"tgemm_transpose_f32": lambda a, b: tgemm.tgemm_transpose_f32(a, b, stream),
@@ -409,10 +507,10 @@ def bench_tgemm(args, world, rank, local):
                     ev.append((e0, e1))
                 torch.cuda.synchronize(dev)
                 ts = [a.elapsed_time(b) / 1e3 for a, b in ev[args.warmup:]]
-                avg = sum(ts) / len(ts)
-                gbs = 2 * nbytes / avg / 1e9
+                med = statistics.median(ts)
+                gbs = 2 * nbytes / med / 1e9
                 transposes[f"{name}_{rows}x{cols}"] = {
-                    "us": round(avg * 1e6, 2), "GB_s": round(gbs, 1),
+                    "us": round(med * 1e6, 2), "GB_s": round(gbs, 1),
                     "frac_of_hbm": round(gbs / float(peaks["hbm_gbs"]), 4)}
             del srcs, dst
 
@@ -452,7 +550,8 @@ def bench_tgemm(args, world, rank, local):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps, world)
-        e2e = {"value": round(world * flops_step / e2e_s / 1e12, 3), "unit": UNIT,
+        e2e_value = flops_step / e2e_s / 1e12 if shard_rows else world * flops_step / e2e_s / 1e12
+        e2e = {"value": round(e2e_value, 3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e2e_s * 1e3, 3)}
 
@@ -469,13 +568,12 @@ def bench_tgemm(args, world, rank, local):
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32",
+                "scaling": "strong" if shard_rows else "weak", "vs_baseline": None, "dtype": "bf16+f32",
                 "data": "synthetic (seeded SplitMix64; bf16 N(0,1)/sqrt(k), fp32 N(0,1))",
-                "config": {"workload": "gemm 8192x8192x8192 bf16->fp32 (tcgen05) + 4096x4096x4096 fp32 (FFMA)",
-                           "l2": "inputs larger than L2: each launch reads the next of R input copies (>= 384 MiB per shape)",
-                           "parallelism": f"replicas x{world}"},
+                "config": step_config(world, shard_rows),
                 "roofline": roof, "parts": parts, "transposes": transposes, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": int(launches), "clocks": clocks.summary(),
+                "gpu_launches": int(launches), "clocks": clock_summary,
+                "fp32_peak": {"tflops": round(fp32[0], 2), "derivation": fp32[1]},
                 "wall_s_timed_region": round(t_wall, 3), "impl": "tgemm"}
         print(json.dumps(line), flush=True)
 
@@ -486,6 +584,9 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tgemm", "reference"], default="tgemm")
+    ap.add_argument("--shard", choices=["rows", "replicas"], default="rows",
+                    help="N > 1: split each product's rows across the ranks (strong scaling, default) "
+                         "or run the whole step on every rank (weak scaling)")
     ap.add_argument("--no-extras", action="store_true", help="skip the informational extra shapes")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")

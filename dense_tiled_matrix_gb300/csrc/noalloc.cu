@@ -135,6 +135,9 @@ extern "C" tgemm_status tgemm_tf32_noalloc(int64_t m, int64_t n, int64_t k, cons
         p.ldb = k4;
     }
     if (err == cudaSuccess) err = launch_umma(p, *dev, true, nullptr);   // whole tiles: no partial-sum workspace
-    if (err != cudaSuccess) return TGEMM_ERR_CUDA;
+    if (err != cudaSuccess) {
+        if (tgemm_last_error()[0] == '\0') set_error("CUDA: %s", cudaGetErrorString(err));
+        return TGEMM_ERR_CUDA;
+    }
     return TGEMM_OK;
 }

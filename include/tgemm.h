@@ -132,9 +132,13 @@ tgemm_status tgemm_transpose_f32(int64_t rows, int64_t cols,
 #define TGEMM_NOALLOC_SCRATCH_BYTES (32ull << 20)
 
 /*
- * tgemm_tf32 without allocating.  Same operation, argument rules, results and
- * status codes as tgemm_tf32 (the pages have no counterpart: this concerns only
- * where the library keeps its temporary data).
+ * tgemm_tf32 without allocating.  Same operation, argument rules and status
+ * codes as tgemm_tf32 (the pages have no counterpart: this concerns only where
+ * the library keeps its temporary data).  It never splits an output tile along
+ * k between CTAs, so on shapes where tgemm_tf32 does (a partly filled last
+ * wave of tiles) the k terms are added in another order: the results agree
+ * with tgemm_tf32 within the TF32 error bound, exactly on integer-valued
+ * inputs, and may take longer there.
  *
  * Who needs it: callers that cannot let a library allocate device memory --
  * programs whose device memory is wholly managed by their own allocator or a

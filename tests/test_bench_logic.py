@@ -20,25 +20,62 @@ def test_skinny_bf16_is_hbm_bound_on_algorithmic_bytes():
     assert r["frac"] == pytest.approx(r["achieved"] / 6792.0, abs=1e-4)
 
 
-@pytest.mark.parametrize("entry, bound, peak", [
-    ("f32", "alu", 152 * 128 * 2 * 2070e6 / 1e12),
-    ("pages_naive", "alu", 152 * 128 * 2 * 2070e6 / 1e12),
-    ("bf16", "tensor", 1904.1),
-    ("tf32", "tensor", 1904.1 * 1100.0 / 2250.0),
+@pytest.mark.parametrize("entry, bound, peak, nominal", [
+    ("f32", "alu", 148 * 128 * 2 * 1980e6 / 1e12, None),
+    ("pages_naive", "alu", 148 * 128 * 2 * 1980e6 / 1e12, None),
+    ("bf16", "tensor", 1904.1, 2250.0),
+    ("tf32", "tensor", 1904.1 * 1100.0 / 2250.0, 1100.0),
 ])
-def test_compute_bound_paths_use_their_own_peak(entry, bound, peak):
+def test_compute_bound_paths_use_their_own_peak(entry, bound, peak, nominal):
     c = Case(4096, 4096, 4096)
-    r = bench.roofline_for(entry, c, 2.0e-3, PEAKS, "measured")
+    fp32 = bench.fp32_peak(148, 1980.0)      # SM count and clock as read at run time
+    r = bench.roofline_for(entry, c, 2.0e-3, PEAKS, "measured", fp32)
     flops = 2.0 * 4096 ** 3
     assert r["bound"] == bound and r["unit"] == "TFLOP/s" and r["algorithmic_flops"] == int(flops)
     assert r["peak"] == pytest.approx(peak, abs=0.01)
     assert r["achieved"] == pytest.approx(flops / 2.0e-3 / 1e12, abs=0.01)
     assert r["frac"] == pytest.approx(flops / 2.0e-3 / 1e12 / peak, abs=1e-4)
+    if nominal is None:
+        assert "148 SMs" in r["peak_source"] and "1980 MHz" in r["peak_source"]
+        assert "frac_of_nominal" not in r
+    else:
+        assert r["nominal_peak"] == nominal
+        assert r["frac_of_nominal"] == pytest.approx(flops / 2.0e-3 / 1e12 / nominal, abs=1e-4)
+
+
+def test_fp32_peak_derivation():
+    tf, how = bench.fp32_peak(152, 2070.0)
+    assert tf == pytest.approx(152 * 128 * 2 * 2070e6 / 1e12)
+    assert how.startswith("152 SMs x 128 FP32 lanes x 2 flop x 2070 MHz")
+
+
+def test_traffic_table_parses_and_matches_its_sources():
+    """Every row of the committed ncu traffic table parses; a row whose kernel
+    sources are unchanged gives its bytes, a changed one gives None."""
+    table = bench.traffic_table()
+    assert {"f32_4096", "bf16_8192"} <= set(table)
+    for part, row in table.items():
+        assert row["source"].startswith("profiles/")
+        if not row["stale"]:
+            assert isinstance(row["bytes"], int) and row["bytes"] > 0, part
+        else:
+            assert row["bytes"] is None, part
+
+
+def test_traffic_table_marks_changed_sources_stale(tmp_path):
+    path = tmp_path / "t.csv"
+    digest = bench.source_digest(["ffma_f32.cu"])
+    path.write_text("# comment\npart,bytes_per_call,kernels,sources,sha256_16,summary\n"
+                    f"a,100,k,ffma_f32.cu,{digest},profiles/x.md\n"
+                    "b,200,k,ffma_f32.cu,0000000000000000,profiles/y.md\n")
+    table = bench.traffic_table(str(path))
+    assert table["a"] == {"bytes": 100, "source": "profiles/x.md (k)", "stale": False}
+    assert table["b"]["bytes"] is None and table["b"]["stale"]
 
 
 def _summary(tmp_path, lines):
     s = bench.ClockSampler(0)
-    s.path = os.path.join(tmp_path, "clocks.csv")
+    s.path = os.path.join(tmp_path, "clocks.csv")   # as if __enter__ had made it
     with open(s.path, "w") as fh:
         fh.write("\n".join(lines) + "\n")
     s.proc = object()   # as if nvidia-smi had run

@@ -5,10 +5,15 @@ static device array of TGEMM_NOALLOC_SCRATCH_BYTES instead.
 
 The test calls the entry point through the C ABI twice in a row, with
 different shapes (the second needs a re-pitched A as well as the transposed B,
-so it reuses the array the first call wrote), and checks each output against
-tgemm_tf32 on the same inputs, within the TF32 bound the other parity tests
-use: max |C_noalloc - C_tf32| / (|A| |B|) <= 4e-3.  It also checks that a
-shape too large for the array is refused before any work is queued.
+so it reuses the array the first call wrote), and checks each output element
+by element against the CPU oracle (hecess.blogspot.com "[Multi-Core & GPU
+Programming] CUDA - Matrix Multiplication", section "[Matrix
+Multiplication]": P(i,j) = sum_k M(i,k) N(k,j)):
+  * integer-valued inputs whose sums are exact in fp32 must match exactly;
+  * N(0,1) inputs within the TF32 bound max |C - P| / (|A| |B|) <= 4e-3.
+As an extra check the output is also compared with tgemm_tf32 on the same
+inputs.  A shape too large for the array must be refused before any work is
+queued.
 
 This file is named so that pytest collects it last; it passes alone in a fresh
 process and after the rest of the suite.
@@ -45,28 +50,47 @@ def _raw_call(name, A, B, C, lda):
               ctypes.c_void_p(C.data_ptr()), C.stride(0), ctypes.c_void_p(stream))
 
 
-def _compare(m, n, k, seed, a_pad):
-    case = inputs.random_case(seed, m, n, k, kind="normal")
-    # A with a leading dimension of k + a_pad (a_pad = 1 makes lda*4 not a multiple of 16)
+def _run(name, case, a_pad):
+    """C from entry point `name` with A stored at a leading dimension of k + a_pad
+    (a_pad = 1 makes lda * 4 not a multiple of 16, so A is re-pitched)."""
+    m, n, k = case.m, case.n, case.k
     A_store = torch.zeros((m, k + a_pad), dtype=torch.float32, device="cuda")
     A_store[:, :k] = torch.from_numpy(case.A).cuda()
     A = A_store[:, :k]
     B = torch.from_numpy(case.B).cuda()
-    C_ref = torch.full((m, n), float("nan"), device="cuda")
-    C_new = torch.full((m, n), float("nan"), device="cuda")
-    assert _raw_call("tgemm_tf32", A, B, C_ref, k + a_pad) == tgemm.TGEMM_OK, tgemm.tgemm_last_error()
-    assert _raw_call("tgemm_tf32_noalloc", A, B, C_new, k + a_pad) == tgemm.TGEMM_OK, tgemm.tgemm_last_error()
+    C = torch.full((m, n), float("nan"), device="cuda")
+    status = _raw_call(name, A, B, C, k + a_pad)
+    assert status == tgemm.TGEMM_OK, f"{name}: {tgemm.tgemm_status_string(status)}: {tgemm.tgemm_last_error()}"
     torch.cuda.synchronize()
-    _, D = oracle.gemm(case.A, case.B)
-    diff = np.abs(C_new.cpu().numpy().astype(np.float64) - C_ref.cpu().numpy().astype(np.float64))
-    assert np.all(np.isfinite(diff)), "non-finite output"
-    err = float(np.max(diff / D))
-    assert err <= TOL_TF32, f"tgemm_tf32_noalloc vs tgemm_tf32: {err:.3e}"
+    return C.cpu().numpy().astype(np.float64)
 
 
-def test_noalloc_matches_tgemm_tf32_on_two_calls_in_a_row():
-    _compare(1000, 700, 900, seed=9001, a_pad=0)     # transposed B in the array
-    _compare(333, 517, 301, seed=9002, a_pad=1)      # re-pitched A and transposed B
+def _check_against_oracle(m, n, k, seed, a_pad, kind):
+    case = inputs.random_case(seed, m, n, k, kind=kind)
+    got = _run("tgemm_tf32_noalloc", case, a_pad)
+    P, D = oracle.gemm(case.A, case.B)
+    assert np.all(np.isfinite(got)), "non-finite output"
+    if case.exact:
+        ref = P.astype(np.float32).astype(np.float64)
+        bad = np.argwhere(got != ref)
+        assert bad.size == 0, f"{len(bad)} elements differ from the oracle's exact sums, first {bad[:3].tolist()}"
+    else:
+        diff = np.abs(got - P)
+        zero = D == 0
+        assert np.all(diff[zero] == 0)
+        err = float(np.max(diff[~zero] / D[~zero]))
+        assert err <= TOL_TF32, f"tgemm_tf32_noalloc vs oracle: {err:.3e}"
+    # extra check: the allocating entry point agrees within the same bound
+    other = _run("tgemm_tf32", case, a_pad)
+    err_other = float(np.max(np.abs(got - other) / np.where(D == 0, 1.0, D)))
+    assert err_other <= TOL_TF32, f"tgemm_tf32_noalloc vs tgemm_tf32: {err_other:.3e}"
+
+
+@pytest.mark.parametrize("kind", ["int", "normal"])
+def test_noalloc_matches_oracle_on_two_calls_in_a_row(kind):
+    base = 9001 if kind == "int" else 9101
+    _check_against_oracle(1000, 700, 900, seed=base, a_pad=0, kind=kind)     # transposed B in the array
+    _check_against_oracle(333, 517, 301, seed=base + 1, a_pad=1, kind=kind)  # re-pitched A and transposed B
     assert tgemm.tgemm_get_device_status() == tgemm.TGEMM_OK
 
 
