@@ -422,8 +422,12 @@ def bench_tgemm(args, world, rank, local):
             out[name] = e0.elapsed_time(e1) / 1e3 / iters
         return out
 
-    runs = {name: prepare(spec, shard_rows) for name, spec in PARTS.items()}
-    extras = {} if args.no_extras or rank != 0 else {name: prepare(spec, False) for name, spec in EXTRAS.items()}
+    only = set(args.only.split(",")) if args.only else None
+    if only and not only <= set(PARTS) | set(EXTRAS):
+        raise SystemExit(f"--only: unknown parts {sorted(only - set(PARTS) - set(EXTRAS))}")
+    runs = {name: prepare(spec, shard_rows) for name, spec in PARTS.items() if not only or name in only}
+    extras = {} if args.no_extras or rank != 0 else {name: prepare(spec, False) for name, spec in EXTRAS.items()
+                                                     if not only or name in only}
 
     with ClockSampler(local) as clocks:
         timed(runs, args.warmup)
@@ -442,7 +446,7 @@ def bench_tgemm(args, world, rank, local):
         b2b = back_to_back(runs, args.steps)
         b2b.update(back_to_back({n: r for n, r in extras.items() if n not in slow}, args.steps))
     clock_summary = clocks.summary()
-    step_s = sum(sum(v) for v in per.values()) / args.steps
+    step_s = max(sum(sum(v) for v in per.values()) / args.steps, 1e-12)
     step_s = max_over_ranks(step_s, world)
     if shard_rows:
         # the full products' flops: the ranks' row blocks together cover every row once
@@ -475,16 +479,19 @@ def bench_tgemm(args, world, rank, local):
             # informational: `ms`, `tflops` and the roofline use the per-launch event pairs
             parts[name]["ms_back_to_back"] = round(b2b[name] * 1e3, 4)
             parts[name]["roofline_frac_back_to_back"] = round(roof_part["frac"] * med / b2b[name], 4)
-    dominant = max(PARTS, key=lambda n: sum(per[n]))
-    roof = dict(parts[dominant]["roofline"])
-    roof["kernel"] = KERNEL_NAMES[PARTS[dominant][1]]
-    roof["workload"] = dominant
+    if runs:
+        dominant = max(runs, key=lambda n: sum(per[n]))
+        roof = dict(parts[dominant]["roofline"])
+        roof["kernel"] = KERNEL_NAMES[PARTS[dominant][1]]
+        roof["workload"] = dominant
+    else:
+        roof = None   # --only without a part of the step: no step, no step roofline
 
     # The lecture's transpose case study (naive -> coalesced shared tile ->
     # padded tile) next to libtgemm's transpose, at the lecture's 1024 x 1024
     # and at 16384 x 16384 (HBM-bound); GB/s counts the bytes read and written.
     transposes = {}
-    if extras:
+    if extras and not only:
         gen = torch.Generator(device=dev)
         gen.manual_seed(1006)
         kernels = {"tgemm_transpose_f32": lambda a, b: tgemm.tgemm_transpose_f32(a, b, stream),
@@ -516,7 +523,7 @@ def bench_tgemm(args, world, rank, local):
 
     # End to end through the C ABI: pinned host inputs -> device, product, result -> host.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and runs:
         host = {}
         h2d = d2h = 0
         for name, (c, copies, C, fn) in runs.items():
@@ -560,7 +567,7 @@ def bench_tgemm(args, world, rank, local):
         raise RuntimeError(f"device status after the bench: {tgemm.tgemm_status_string(status)}")
 
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not only:
         flops, dt, rows, cores = cpu_sample([case_of(PARTS[p][0]) for p in PARTS], target_s=args.cpu_seconds)
         cpu = {"value": flops / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"first {rows} rows of each of the step's two products (fp64 oracle), {dt:.1f} s"}
@@ -588,6 +595,8 @@ def main():
                     help="N > 1: split each product's rows across the ranks (strong scaling, default) "
                          "or run the whole step on every rank (weak scaling)")
     ap.add_argument("--no-extras", action="store_true", help="skip the informational extra shapes")
+    ap.add_argument("--only", default="", help="profiling aid: time only these comma-separated parts "
+                                                "(names of `parts` in the JSON line); no CPU baseline")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffer) measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip timing the CPU oracle")
     ap.add_argument("--cpu-seconds", type=float, default=20.0, help="target length of the CPU-oracle sample")

@@ -19,6 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libtgemm.so")
+DEBUG_LIB_PATH = os.path.join(PKG, "libtgemm_debug.so")   # with the device-side checks (TGEMM_DEBUG)
 PAGES_DIR = os.path.join(PKG, "csrc_pages")
 PAGES_LIB_PATH = os.path.join(PKG, "libtgemm_pages.so")
 
@@ -54,7 +55,7 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _build_lib(srcs, lib_path, tag, verbose, force, ptxas_verbose):
+def _build_lib(srcs, lib_path, tag, verbose, force, ptxas_verbose, extra=()):
     os.makedirs(BUILD_DIR, exist_ok=True)
     cc = nvcc()
     headers = _headers()
@@ -64,7 +65,7 @@ def _build_lib(srcs, lib_path, tag, verbose, force, ptxas_verbose):
         obj = os.path.join(BUILD_DIR, tag + "_" + os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src, *headers, __file__]):
-            cmd = [cc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+            cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
             if ptxas_verbose:
                 cmd[1:1] = ["-Xptxas", "-v"]
             jobs.append(cmd)
@@ -93,12 +94,17 @@ def _build_lib(srcs, lib_path, tag, verbose, force, ptxas_verbose):
 
 
 def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False) -> str:
-    """Compile and link ``libtgemm.so`` (and the pages' comparator library); returns libtgemm's path."""
-    with ThreadPoolExecutor(max_workers=2) as pool:
+    """Compile and link ``libtgemm.so``, its debug build ``libtgemm_debug.so``
+    (the same sources with the device-side consistency checks, TGEMM_DEBUG) and
+    the pages' comparator library; returns libtgemm's path."""
+    with ThreadPoolExecutor(max_workers=3) as pool:
         main = pool.submit(_build_lib, sources(), LIB_PATH, "tgemm", verbose, force, ptxas_verbose)
+        debug = pool.submit(_build_lib, sources(), DEBUG_LIB_PATH, "tgemm_dbg", verbose, force, ptxas_verbose,
+                            ("-DTGEMM_DEBUG",))
         pages = pool.submit(_build_lib, sources(PAGES_DIR), PAGES_LIB_PATH, "pages", verbose, force,
                             ptxas_verbose)
         pages.result()
+        debug.result()
         return main.result()
 
 

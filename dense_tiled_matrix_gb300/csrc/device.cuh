@@ -18,7 +18,32 @@ namespace tgemm {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
 // Status word values written by kernels (host side maps them to tgemm_status).
+// The low byte is the code; a failed debug check also records where it sits
+// (file id in bits 8-11, source line from bit 12).
 constexpr uint32_t kStatusTimeout = 5u;
+constexpr uint32_t kStatusDebugCheck = 7u;
+
+// File ids of the debug checks.
+constexpr uint32_t kFileFfma = 1, kFileUmma = 2, kFileSkinny = 3, kFileTranspose = 4, kFileSelftest = 5;
+
+// Records a failed consistency check in the status word (the first failure
+// is kept).  Used by the checks of debug builds and by the self-test.
+__device__ __forceinline__ void debug_fail(uint32_t* status, uint32_t file, uint32_t line) {
+    atomicCAS(status, 0u, kStatusDebugCheck | (file << 8) | (line << 12));
+}
+
+// Device-side consistency checks of the debug build (-DTGEMM_DEBUG): the
+// condition is evaluated, a failure is recorded with its file and line, and
+// the caller skips the access the check guards.  In normal builds the checks
+// compile to nothing and always pass.
+#ifdef TGEMM_DEBUG
+#define TGEMM_DCHECK(cond, status, file) \
+    ((cond) ? true : (::tgemm::debug_fail((status), (file), static_cast<uint32_t>(__LINE__)), false))
+constexpr bool kDebugBuild = true;
+#else
+#define TGEMM_DCHECK(cond, status, file) true
+constexpr bool kDebugBuild = false;
+#endif
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -207,10 +207,20 @@ ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     constexpr int kBM = F::BM;
     extern __shared__ uint8_t smem_raw[];
     const Smem sm(smem_raw);
+#ifdef TGEMM_DEBUG
+    // Debug build: how often each stage was filled (producer) and released
+    // (one count per consumer warp), to check every wait's phase.
+    __shared__ uint32_t dbg_fills[kStages], dbg_releases[kStages];
+#endif
     const int warp_all = threadIdx.x >> 5;
-    // The next launch of a split product (pieces after whole tiles, the reduce
-    // after the pieces) may start on SMs this grid frees; it reads nothing this
-    // grid writes (the reduce waits for the pieces on the device).
+    // A whole-tile grid is launched as a programmatic dependent of the kernel
+    // before it (e.g. the re-pitch of a misaligned operand): every thread
+    // waits here until that kernel has completed, before any global access.
+    // Only then may the next launch of a split product (the pieces after the
+    // whole tiles, the reduce after the pieces) start on SMs this grid frees;
+    // it reads nothing this grid writes (the reduce waits for the pieces on
+    // the device, the pieces for this grid at their end).
+    if (parts == 1) griddep_wait();
     griddep_launch_dependents();
     const int lane = threadIdx.x & 31;
     // Tile origin and k-range of this block (recomputed where needed rather
@@ -234,6 +244,10 @@ ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], F::WARPS);
+#ifdef TGEMM_DEBUG
+            dbg_fills[s] = 0;
+            dbg_releases[s] = 0;
+#endif
         }
         fence_barrier_init();
     }
@@ -251,6 +265,11 @@ ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 const int s = i % kStages;
                 if (i >= kStages && !mbar_wait(&sm.empty[s], static_cast<uint32_t>(i / kStages - 1) & 1u, status))
                     break;   // the consumers time out on the stages never filled
+#ifdef TGEMM_DEBUG
+                // every consumer warp has released every earlier fill of this stage
+                TGEMM_DCHECK(dbg_releases[s] == static_cast<uint32_t>(i / kStages) * F::WARPS, status, kFileFfma);
+                dbg_fills[s] = static_cast<uint32_t>(i / kStages) + 1;
+#endif
                 mbar_arrive_expect_tx(&sm.full[s], F::STAGE_A + kStageB);
                 tma_load_2d(sm.sA + s * (kBM * kBK), &tmA, &sm.full[s], (k0 + i) * kBK, m0);
                 tma_load_2d(sm.sB + s * (kBK * kBN), &tmB, &sm.full[s], n0, (k0 + i) * kBK);
@@ -277,6 +296,13 @@ ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     // 64-byte swizzle: 16-byte chunk c of tile row r sits at chunk c ^ ((r >> 1) & 3).
     // For r = a_row0 + 4i this is (tm >> 1) ^ (2 * (i & 1)).
     const int swz_even = kBK == 16 ? (tm >> 1) : tm;
+    // The thread's shared-memory reads stay inside a stage: A rows a_row0 + 4i
+    // (i < kTR), swizzled 16-byte chunks < kBK / 4; B columns b_col0 .. +3 and
+    // b_col0 + 32 .. +35.
+    if (!TGEMM_DCHECK(a_row0 + 4 * (kTR - 1) < kBM && (swz_even ^ (kBK == 16 ? 3 : 7)) < kBK / 4 &&
+                          b_col0 + 32 + 3 < kBN,
+                      status, kFileFfma))
+        return;
     int k0, NI;
     k_range(k0, NI);
     Acc acc;
@@ -285,9 +311,18 @@ ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     uint32_t phase = 0;
     for (int i = 0; i < NI; ++i) {
         if (!mbar_wait(&sm.full[s], phase, status)) return;   // status records the timeout
+#ifdef TGEMM_DEBUG
+        // the stage holds fill i / kStages: neither an older one nor a refill
+        TGEMM_DCHECK(dbg_fills[s] == static_cast<uint32_t>(i / kStages) + 1, status, kFileFfma);
+#endif
         fma_phase(acc, sm.sA + s * (kBM * kBK), sm.sB + s * (kBK * kBN), a_row0, b_col0, swz_even);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[s]);
+        if (lane == 0) {
+#ifdef TGEMM_DEBUG
+            atomicAdd(&dbg_releases[s], 1u);
+#endif
+            mbar_arrive(&sm.empty[s]);
+        }
         if (++s == kStages) { s = 0; phase ^= 1u; }
     }
     if (parts == 1) {
@@ -309,37 +344,63 @@ ffma_f32_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 }
 
 // C of the remainder tiles: tile tile0 + b is the sum of the pieces in
-// slots b * parts .. b * parts + parts - 1, added in part order.
+// slots b * parts .. b * parts + parts - 1, added in part order.  Four blocks
+// share a tile, one per 32-row quarter (the rows of the piece kernel's
+// consumer warps wm = q): reduce thread t takes consumer thread
+// 64 q + (t % 64)'s float4 slots j = 4 (t / 64) .. +3 (rows a_row0 + 4 (j / 2),
+// columns b_col0 + 32 (j % 2) .. +3), so consecutive threads read consecutive
+// float4s of the workspace and store neighbouring 16-byte pieces of C.
+constexpr int kReduceSplit = 4;
+
 __global__ void __launch_bounds__(FCfg::THREADS)
 ffma_f32_reduce_kernel(const float* __restrict__ ws, float* __restrict__ C, int64_t ldc, int M, int N, int tile0,
                        int parts, int vec_store) {
     using F = FCfg;
     constexpr int kBM = F::BM;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int kSlots = kTR * 2;                         // float4 slots per consumer thread
+    constexpr int kPer = kSlots * 64 / F::THREADS;          // slots per reduce thread (4)
+    const int tile = static_cast<int>(blockIdx.x) / kReduceSplit;
+    const int q = static_cast<int>(blockIdx.x) % kReduceSplit;
+    const int src = 64 * q + (threadIdx.x & 63);             // consumer thread whose slots this thread adds
+    const int j0 = (threadIdx.x >> 6) * kPer;
+    const int warp = src >> 5, lane = src & 31;
     const int wm = warp >> 1, wn = warp & 1;
     const int tm = lane >> 3, tn = lane & 7;
     const int a_row0 = 4 * kTR * wm + tm;
     const int b_col0 = 64 * wn + 4 * tn;
     int tile_m, tile_n;
-    tile_coords(tile0 + blockIdx.x, (M + kBM - 1) / kBM, (N + kBN - 1) / kBN, tile_m, tile_n);
+    tile_coords(tile0 + tile, (M + kBM - 1) / kBM, (N + kBN - 1) / kBN, tile_m, tile_n);
     griddep_wait();   // the pieces have been written (launched as their dependent)
-    Acc acc;
-    zero(acc);
-    const float4* src = reinterpret_cast<const float4*>(ws + static_cast<int64_t>(blockIdx.x) * parts * kBM * kBN) + tid;
-    for (int q = 0; q < parts; ++q) {
+    float4 acc[kPer];
 #pragma unroll
-        for (int i = 0; i < kTR; ++i)
+    for (int j = 0; j < kPer; ++j) acc[j] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    const float4* slot = reinterpret_cast<const float4*>(ws + static_cast<int64_t>(tile) * parts * kBM * kBN) + src;
+    for (int p = 0; p < parts; ++p) {
 #pragma unroll
-            for (int p = 0; p < 4; p += 2) {
-                const float4 v = __ldcs(src + (i * 2 + p / 2) * F::THREADS);
-                acc[i][p].x += v.x;
-                acc[i][p].y += v.y;
-                acc[i][p + 1].x += v.z;
-                acc[i][p + 1].y += v.w;
-            }
-        src += kBM * kBN / 4;
+        for (int j = 0; j < kPer; ++j) {
+            const float4 v = __ldcs(slot + (j0 + j) * F::THREADS);
+            acc[j].x += v.x;
+            acc[j].y += v.y;
+            acc[j].z += v.z;
+            acc[j].w += v.w;
+        }
+        slot += kBM * kBN / 4;
     }
-    store_tile(acc, C, ldc, M, N, tile_m * kBM, tile_n * kBN, a_row0, b_col0, vec_store);
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+        const int gm = tile_m * kBM + a_row0 + 4 * ((j0 + j) >> 1);
+        const int gn = tile_n * kBN + b_col0 + 32 * ((j0 + j) & 1);
+        if (gm >= M) continue;
+        float* crow = C + static_cast<int64_t>(gm) * ldc;
+        if (vec_store && gn + 3 < N) {
+            *reinterpret_cast<float4*>(crow + gn) = acc[j];
+        } else {
+            const float v[4] = {acc[j].x, acc[j].y, acc[j].z, acc[j].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (gn + e < N) crow[gn + e] = v[e];
+        }
+    }
 }
 
 // The warp-specialised 128-row kernel over `grid` blocks (see its comment).
@@ -426,7 +487,7 @@ cudaError_t launch_tiles(const Problem& p, const Device& dev) {
     CUtensorMap ta, tb;
     if (!make_maps(p, &ta, &tb)) return cudaErrorInvalidValue;
     const int64_t tiles = static_cast<int64_t>((p.m + F::BM - 1) / F::BM) * ((p.n + kBN - 1) / kBN);
-    cudaError_t err = launch_ws(p, ta, tb, tiles, 0, 1, nullptr, vec_store_ok(p), dev, false);
+    cudaError_t err = launch_ws(p, ta, tb, tiles, 0, 1, nullptr, vec_store_ok(p), dev, true);
     if (err == cudaSuccess) err = cudaGetLastError();
     if (err != cudaSuccess) set_error("ffma_f32_ws_kernel launch: %s", cudaGetErrorString(err));
     return err;
@@ -443,11 +504,11 @@ cudaError_t launch_split_tail(const Problem& p, const Device& dev, void* workspa
     const int vec_store = vec_store_ok(p);
     float* ws = static_cast<float*>(workspace);
     cudaError_t err = cudaSuccess;
-    // Whole tiles first (an ordinary launch: everything before it in the
-    // stream has completed), then the pieces of the remainder, which read only
-    // A and B and so start as soon as the whole-tile grid frees SMs, then the
-    // reduce, which waits on the device for the pieces.
-    if (st.full > 0) err = launch_ws(p, ta, tb, st.full, 0, 1, nullptr, vec_store, dev, false);
+    // Whole tiles first (a dependent launch whose CTAs wait for the kernel
+    // before them), then the pieces of the remainder, which read only A and B
+    // and so start as soon as the whole-tile grid frees SMs, then the reduce,
+    // which waits on the device for the pieces.
+    if (st.full > 0) err = launch_ws(p, ta, tb, st.full, 0, 1, nullptr, vec_store, dev, true);
     if (err == cudaSuccess)
         err = launch_ws(p, ta, tb, st.rest * st.parts, st.full, st.parts, ws, vec_store, dev, st.full > 0);
     if (err != cudaSuccess) {
@@ -455,7 +516,8 @@ cudaError_t launch_split_tail(const Problem& p, const Device& dev, void* workspa
         return err;
     }
     cudaLaunchAttribute attr[1];
-    const cudaLaunchConfig_t cfg = launch_config(p, static_cast<unsigned>(st.rest), F::THREADS, 0, true, attr);
+    const cudaLaunchConfig_t cfg =
+        launch_config(p, static_cast<unsigned>(st.rest * kReduceSplit), F::THREADS, 0, true, attr);
     err = cudaLaunchKernelEx(&cfg, ffma_f32_reduce_kernel, static_cast<const float*>(ws), p.C, p.ldc, p.m, p.n,
                              static_cast<int>(st.full), st.parts, vec_store);
     count_launch();

@@ -97,9 +97,19 @@ cudaError_t launch_transpose(const void* src, int64_t ld_src, void* dst, int64_t
                              int64_t cols, cudaStream_t stream, const Device& dev);
 
 // Copies a rows x cols matrix of `elem_bytes`-byte elements with pitch `ld_src`
-// into `dst` with pitch `ld_dst` (elements), zero-filling columns
-// cols .. ld_dst-1.
+// into `dst` with pitch `ld_dst` (elements; dst 16-byte aligned and ld_dst a
+// multiple of 16 bytes), zero-filling columns cols .. ld_dst-1.
 cudaError_t launch_pack(const void* src, int64_t ld_src, void* dst, int64_t ld_dst, int64_t rows,
                         int64_t cols, int elem_bytes, cudaStream_t stream, const Device& dev);
+
+// One or two such copies (same element size) in one launch.
+struct PackSpec {
+    const void* src;
+    int64_t ld_src;
+    void* dst;
+    int64_t ld_dst;
+    int64_t rows, cols;
+};
+cudaError_t launch_pack2(const PackSpec* specs, int count, int elem_bytes, cudaStream_t stream, const Device& dev);
 
 }  // namespace tgemm

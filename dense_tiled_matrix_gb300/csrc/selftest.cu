@@ -42,3 +42,26 @@ extern "C" tgemm_status tgemm_selftest_wait_timeout(int64_t limit_ns, struct CUs
     if (err != cudaSuccess) return cuda_fail("wait_forever_kernel launch", err);
     return TGEMM_OK;
 }
+
+namespace tgemm {
+namespace {
+
+__global__ void record_check_kernel(uint32_t* status) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) debug_fail(status, kFileSelftest, static_cast<uint32_t>(__LINE__));
+}
+
+}  // namespace
+}  // namespace tgemm
+
+extern "C" tgemm_status tgemm_selftest_debug_check(struct CUstream_st* stream) {
+    using namespace tgemm;
+    clear_error();
+    Device* dev = nullptr;
+    tgemm_status st = current_device(&dev);
+    if (st != TGEMM_OK) return st;
+    record_check_kernel<<<1, 32, 0, stream>>>(dev->status);
+    count_launch();
+    const cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return cuda_fail("record_check_kernel launch", err);
+    return TGEMM_OK;
+}

@@ -8,6 +8,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "device.cuh"
 #include "host.h"
 #include "tgemm.h"
 
@@ -265,17 +266,21 @@ tgemm_status run(Kind kind, int64_t m, int64_t n, int64_t k, const void* A, int6
             return TGEMM_ERR_WORKSPACE;
         }
         uint8_t* w = static_cast<uint8_t*>(work);
+        PackSpec specs[2];
+        int packs = 0;
         if (pack_a) {
-            err = launch_pack(A, lda, w, a_ld2, m, k, es, stream, *dev);
+            specs[packs++] = PackSpec{A, lda, w, a_ld2, m, k};
             p.A = w;
             p.lda = a_ld2;
         }
-        if (err == cudaSuccess && transpose_b) {
-            err = launch_transpose(B, ldb, w + b_off, b_ld2, k, n, stream, *dev);
+        if (pack_b) {
+            specs[packs++] = PackSpec{B, ldb, w + b_off, b_ld2, k, n};
             p.B = w + b_off;
             p.ldb = b_ld2;
-        } else if (err == cudaSuccess && pack_b) {
-            err = launch_pack(B, ldb, w + b_off, b_ld2, k, n, es, stream, *dev);
+        }
+        if (packs > 0) err = launch_pack2(specs, packs, es, stream, *dev);   // both operands in one launch
+        if (err == cudaSuccess && transpose_b) {
+            err = launch_transpose(B, ldb, w + b_off, b_ld2, k, n, stream, *dev);
             p.B = w + b_off;
             p.ldb = b_ld2;
         }
@@ -406,6 +411,7 @@ const char* tgemm_status_string(tgemm_status status) {
         case TGEMM_ERR_CUDA: return "CUDA error";
         case TGEMM_ERR_TIMEOUT: return "kernel pipeline wait timed out";
         case TGEMM_ERR_WORKSPACE: return "workspace allocation failed";
+        case TGEMM_ERR_INTERNAL: return "device-side consistency check failed";
     }
     return "unknown status";
 }
@@ -426,6 +432,13 @@ tgemm_status tgemm_get_device_status(struct CUstream_st* stream) {
         const uint32_t zero = 0;
         err = cudaMemcpyToSymbol(g_tgemm_status, &zero, sizeof zero);
         if (err != cudaSuccess) return tgemm::cuda_fail("clearing the status word", err);
+        if ((value & 0xFFu) == tgemm::kStatusDebugCheck) {
+            static const char* const files[] = {"?", "ffma_f32.cu", "umma.cu", "umma_skinny.cu", "transpose.cu",
+                                                "selftest.cu"};
+            const uint32_t file = (value >> 8) & 0xFu;
+            tgemm::set_error("device check failed in %s at line %u", file < 6 ? files[file] : "?", value >> 12);
+            return TGEMM_ERR_INTERNAL;
+        }
         tgemm::set_error("a kernel reported status %u (pipeline wait timed out)", value);
         return TGEMM_ERR_TIMEOUT;
     }
@@ -434,6 +447,8 @@ tgemm_status tgemm_get_device_status(struct CUstream_st* stream) {
 
 uint64_t tgemm_kernel_launches(void) { return tgemm::g_launches.load(std::memory_order_relaxed); }
 
-int tgemm_version(void) { return 100; }
+int tgemm_version(void) { return 200; }
+
+int tgemm_debug_build(void) { return tgemm::kDebugBuild ? 1 : 0; }
 
 }  // extern "C"

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(kTile * kRowsPerPass)
 transpose_kernel(const uint32_t* __restrict__ src, int64_t ld_src, uint32_t* __restrict__ dst,
                  int64_t ld_dst, int rows, int cols) {
     __shared__ uint32_t tile[kTile][kTile + 1];
+    griddep_launch_dependents();   // the product that reads dst may be launched now; it waits for us
     const int tx = threadIdx.x, ty = threadIdx.y;
     const int tiles_c = (cols + kTile - 1) / kTile;
     const int tiles_r = (rows + kTile - 1) / kTile;

@@ -28,8 +28,10 @@
 //    tiles, two accumulators of 256 columns let the epilogue of one tile
 //    overlap the MMAs of the next.
 //  * Warps 2-5 drain an accumulator with tcgen05.ld (warp w reads lanes
-//    32*(w%4) .. +31, i.e. 32 rows of C), and store each row's values with
-//    128-bit stores, masked at the edges of C.
+//    32*(w%4) .. +31, i.e. 32 rows of C, one row per lane), turn each 32 x 32
+//    block through a swizzled shared tile so that a warp store covers whole
+//    128-byte row segments of C (128-bit stores where C's rows are 16-byte
+//    aligned), masked at the edges of C.
 //
 // Every C element is written exactly once.  The tensor cores add the k terms
 // in a fixed order, and a split tile is (head partial) + (tail partial), so
@@ -66,7 +68,9 @@ struct Cfg {
     static constexpr int GROUP_M = kWide ? 8 : 16;
     static constexpr uint32_t IDESC =
         instr_desc(kTF32 ? kFormatTF32 : kFormatBF16, 0, kBKMajor ? 0u : 1u, 128, BN);
-    static constexpr size_t SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + (2 * STAGES + 4) * 8 + 16;
+    // per epilogue warp a 32 x 32 fp32 tile that turns TMEM rows into coalesced row segments of C
+    static constexpr uint32_t EPI_BYTES = 4 * 32 * 32 * 4;
+    static constexpr size_t SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + EPI_BYTES + (2 * STAGES + 4) * 8 + 16;
     static_assert(ACCS * HALVES * 256 <= 512, "accumulators exceed tensor memory");
     static_assert(BN % 32 == 0 && BN <= 256, "tile width");
     static_assert(kBKMajor || BN % CH == 0, "an N-contiguous B tile is a whole number of 128-byte chunks");
@@ -106,12 +110,17 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     uint8_t* smem = smem_align_1024(smem_raw);
     uint8_t* sA = smem;
     uint8_t* sB = smem + G::STAGES * G::A_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(sB + G::STAGES * G::B_BYTES);
+    float* sEpi = reinterpret_cast<float*>(sB + G::STAGES * G::B_BYTES);   // 4 x 32 x 32 fp32
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + G::STAGES * G::B_BYTES + G::EPI_BYTES);
     uint64_t* empty = full + G::STAGES;
     uint64_t* acc_full = empty + G::STAGES;    // [2]
     uint64_t* acc_empty = acc_full + 2;        // [2]
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
     __shared__ int s_flag_ok;
+#ifdef TGEMM_DEBUG
+    // Debug build: the fill number each stage holds, to check every wait's phase.
+    __shared__ uint32_t dbg_fills[G::STAGES];
+#endif
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -152,6 +161,9 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             mbar_init(&acc_full[a], 1);
             mbar_init(&acc_empty[a], 128);
         }
+#ifdef TGEMM_DEBUG
+        for (int s = 0; s < G::STAGES; ++s) dbg_fills[s] = 0;
+#endif
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, G::TMEM_COLS);
@@ -178,6 +190,9 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 tile_coords(tile, tiles_m, tiles_n, G::GROUP_M, tm, tn);
                 for (int kb = ka; kb < kz; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, status)) { ok = false; break; }
+#ifdef TGEMM_DEBUG
+                    dbg_fills[s] = static_cast<uint32_t>(issued / G::STAGES) + 1;
+#endif
                     mbar_arrive_expect_tx(&full[s], G::A_BYTES + G::B_BYTES);
                     tma_load_2d(sA + s * G::A_BYTES, &tmA, &full[s], kb * G::BK, tm * G::BM);
                     uint8_t* b_dst = sB + s * G::B_BYTES;
@@ -204,6 +219,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int it = 0;
             int last_s = -1;   // stage of the last commit to an empty barrier
             uint32_t last_ph = 0;
+            int consumed = 0;   // stages consumed so far (debug checks)
             Seq sq;
             seq_init(sq);
             int tile, ka, kz;
@@ -213,11 +229,24 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 if (!mbar_wait(&acc_empty[acc], acc_ph ^ 1u, status)) break;
                 tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + acc * (G::HALVES * G::TCOL);
+                // the accumulator's columns lie inside the allocation
+                if (!TGEMM_DCHECK((acc * G::HALVES + G::HALVES - 1) * G::TCOL + G::BN <= G::TMEM_COLS, status,
+                                  kFileUmma))
+                    break;
                 for (int kb = ka; kb < kz; ++kb) {
                     if (!mbar_wait(&full[s], ph, status)) { ok = false; break; }
                     tc_fence_after_sync();
                     const uint32_t a0 = smem_addr(sA + s * G::A_BYTES);
                     const uint32_t b0 = smem_addr(sB + s * G::B_BYTES);
+#ifdef TGEMM_DEBUG
+                    // the stage holds fill `consumed / STAGES` (not an older one, not a refill),
+                    // and the last MMA's operands end inside their stage
+                    TGEMM_DCHECK(dbg_fills[s] == static_cast<uint32_t>(consumed / G::STAGES) + 1, status, kFileUmma);
+                    TGEMM_DCHECK(s < G::STAGES && (G::HALVES - 1) * 128 * 128 + (G::BK / G::UK - 1) * 32 + 32 <=
+                                                      static_cast<int>(G::A_BYTES),
+                                 status, kFileUmma);
+#endif
+                    ++consumed;
 #pragma unroll
                     for (int kk = 0; kk < G::BK / G::UK; ++kk) {
                         // B, MN-major: 128-byte chunks of N (CH_BYTES apart), 8-row K
@@ -258,6 +287,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // waiting at a named barrier.
         const int quarter = warp & 3;   // tensor-memory lanes 32*quarter .. +31
         const int row_in_half = quarter * 32 + lane;
+        float* epi = sEpi + (warp - 2) * 32 * 32;   // this warp's 32 x 32 staging tile
         bool ok = true;
         int it = 0;
         Seq sq;
@@ -280,18 +310,24 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             const float4* next_part =
                 reinterpret_cast<const float4*>(ws + static_cast<int64_t>(blockIdx.x + 1) * G::BM * G::BN);
             if (head) {
-                if (threadIdx.x == 64) s_flag_ok = ok && wait_flag(flags + blockIdx.x + 1, status) ? 1 : 0;
+                // a head's tail is the next CTA, which exists
+                if (threadIdx.x == 64)
+                    s_flag_ok = ok && TGEMM_DCHECK(blockIdx.x + 1 < gridDim.x, status, kFileUmma) &&
+                                        wait_flag(flags + blockIdx.x + 1, status)
+                                    ? 1
+                                    : 0;
                 epilogue_sync();
             }
 #pragma unroll
             for (int h = 0; h < G::HALVES; ++h) {
-                const int row = tm * G::BM + h * 128 + row_in_half;
-                float* crow = C + static_cast<int64_t>(row) * ldc;
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        (acc * G::HALVES + h) * G::TCOL;
 #pragma unroll 1
                 for (int c = 0; c < G::BN / 32; ++c) {
                     uint32_t r[32];
+                    // columns of this load inside the allocation (uniform across the warp)
+                    (void)TGEMM_DCHECK((acc * G::HALVES + h) * G::TCOL + c * 32 + 32 <= G::TMEM_COLS, status,
+                                       kFileUmma);
                     tmem_load_32(t_row + c * 32, r);
                     tmem_load_wait();
                     const int slot = (h * (G::BN / 32) + c) * 8;
@@ -313,20 +349,51 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                             r[4 * q + 3] = __float_as_uint(__uint_as_float(r[4 * q + 3]) + v.w);
                         }
                     }
+                    // Corner turn (note.jhbae.stream "Lec 29 · GPU Architecture (2)",
+                    // transpose case study): lane l holds row l of this 32 x 32 block;
+                    // through the warp's shared tile the warp then writes whole row
+                    // segments, 128 contiguous bytes per row, instead of 32 rows at once.
+                    // 16-byte chunk q of tile row i sits at chunk q ^ (i % 8), so the
+                    // row-wise writes and the column-wise reads are conflict-free.
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<float4*>(epi + lane * 32 + ((q ^ (lane & 7)) << 2)) =
+                            make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                        __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                    __syncwarp();
                     const int col0 = tn * G::BN + c * 32;
-                    if (row < M) {
-                        if (vec_store && col0 + 32 <= N) {
+                    const int row0 = tm * G::BM + h * 128 + quarter * 32;
+                    if (vec_store) {
+                        // 4 rows x 128 bytes per warp store
+                        const int q = lane & 7;
+                        const int col = col0 + 4 * q;
 #pragma unroll
-                            for (int j = 0; j < 32; j += 4)
-                                *reinterpret_cast<float4*>(crow + col0 + j) =
-                                    make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                                                __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
-                        } else {
+                        for (int i = 0; i < 8; ++i) {
+                            const int rr = 4 * i + (lane >> 3);
+                            const float4 v = *reinterpret_cast<const float4*>(epi + rr * 32 + ((q ^ (rr & 7)) << 2));
+                            if (row0 + rr < M) {
+                                float* dst = C + static_cast<int64_t>(row0 + rr) * ldc + col;
+                                if (col + 4 <= N) {
+                                    *reinterpret_cast<float4*>(dst) = v;
+                                } else {
+                                    const float e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                if (col0 + j < N) crow[col0 + j] = __uint_as_float(r[j]);
+                                    for (int j = 0; j < 4; ++j)
+                                        if (col + j < N) dst[j] = e[j];
+                                }
+                            }
+                        }
+                    } else {
+                        // one row x 128 bytes per warp store (C rows not 16-byte aligned)
+                        const int col = col0 + lane;
+                        const int q = lane >> 2, w = lane & 3;
+#pragma unroll 8
+                        for (int rr = 0; rr < 32; ++rr) {
+                            const float v = epi[rr * 32 + ((q ^ (rr & 7)) << 2) + w];
+                            if (row0 + rr < M && col < N) C[static_cast<int64_t>(row0 + rr) * ldc + col] = v;
                         }
                     }
+                    __syncwarp();   // the tile is rewritten by the next block
                 }
             }
             tc_fence_before_sync();

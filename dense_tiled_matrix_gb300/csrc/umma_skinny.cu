@@ -72,6 +72,10 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     uint64_t* empty = full + G::STAGES;
     uint64_t* done = empty + G::STAGES;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+#ifdef TGEMM_DEBUG
+    // Debug build: the fill number each stage holds, to check every wait's phase.
+    __shared__ uint32_t dbg_fills[G::STAGES];
+#endif
     // After the k loop the B stages hold this CTA's partial sums:
     // red[t][m][j], sub-tile t, row m of C, column n0 + 128t + j.
     float* red = reinterpret_cast<float*>(sB);
@@ -91,6 +95,9 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     // the block barrier.
     const int prefill = nkb < G::STAGES ? nkb : G::STAGES;
     auto issue = [&](int slot, int kb) {
+#ifdef TGEMM_DEBUG
+        dbg_fills[slot] = static_cast<uint32_t>((kb - kb0) / G::STAGES) + 1;
+#endif
         mbar_arrive_expect_tx(&full[slot], G::STAGE_B + G::STAGE_A);
         uint8_t* b_dst = sB + slot * G::STAGE_B;
 #pragma unroll
@@ -106,6 +113,9 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             mbar_init(&empty[s], 1);
         }
         mbar_init(done, 1);
+#ifdef TGEMM_DEBUG
+        for (int s = 0; s < G::STAGES; ++s) dbg_fills[s] = 0;
+#endif
         fence_barrier_init();
         for (int i = 0; i < prefill; ++i) issue(i, kb0 + i);   // empty slots: no wait needed
     }
@@ -137,6 +147,12 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         for (int i = 0; i < nkb; ++i) {
             if (!mbar_wait(&full[s], ph, status)) { ok = false; break; }
             tc_fence_after_sync();
+#ifdef TGEMM_DEBUG
+            // the stage holds fill i / STAGES (not an older one, not a refill); the
+            // sub-tiles' accumulators lie inside the tensor-memory allocation
+            TGEMM_DCHECK(dbg_fills[s] == static_cast<uint32_t>(i / G::STAGES) + 1, status, kFileSkinny);
+            TGEMM_DCHECK((NT - 1) * G::COLS + NM <= static_cast<int>(G::TMEM_COLS), status, kFileSkinny);
+#endif
             const uint32_t b0 = smem_addr(sB + s * G::STAGE_B);
             const uint32_t a0 = smem_addr(sA + s * G::STAGE_A);
 #pragma unroll
@@ -199,11 +215,15 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     // --------------------------- add the S partials in rank order, store --
     const int rows = M < NM ? M : NM;
     const uint32_t my_red = smem_addr(red);
+    // every rank of the cluster exists and fits the rank-order sum
+    (void)TGEMM_DCHECK(splits <= kMaxSplit && rank < splits, status, kFileSkinny);
     for (int item = static_cast<int>(rank); item < NT * rows; item += static_cast<int>(splits)) {
         const int t = item / rows, mr = item - t * rows;
         const int n = n0 + t * kTileN + static_cast<int>(threadIdx.x);
         const uint32_t off =
             static_cast<uint32_t>(((t * NM + mr) * kTileN + static_cast<int>(threadIdx.x)) * 4);
+        // the partial sum read lies inside the B stages that hold the partials
+        if (!TGEMM_DCHECK(off + 4 <= G::STAGES * G::STAGE_B, status, kFileSkinny)) continue;
         // all remote loads first (they overlap), then the sum in rank order
         float part[kMaxSplit];
 #pragma unroll

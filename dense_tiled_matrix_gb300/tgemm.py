@@ -15,6 +15,8 @@ import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libtgemm.so")
+# The same library built with the device-side consistency checks (TGEMM_DEBUG).
+DEBUG_LIB_PATH = os.path.join(PKG, "libtgemm_debug.so")
 
 TGEMM_OK = 0
 TGEMM_ERR_INVALID_VALUE = 1
@@ -23,6 +25,7 @@ TGEMM_ERR_UNSUPPORTED_DEVICE = 3
 TGEMM_ERR_CUDA = 4
 TGEMM_ERR_TIMEOUT = 5
 TGEMM_ERR_WORKSPACE = 6
+TGEMM_ERR_INTERNAL = 7
 
 # Every symbol declared in include/tgemm.h, with its ctypes signature.
 _I64, _VP = ctypes.c_int64, ctypes.c_void_p
@@ -37,6 +40,8 @@ SIGNATURES = {
     "tgemm_last_error": (ctypes.c_char_p, []),
     "tgemm_get_device_status": (ctypes.c_int, [_VP]),
     "tgemm_selftest_wait_timeout": (ctypes.c_int, [_I64, _VP]),
+    "tgemm_selftest_debug_check": (ctypes.c_int, [_VP]),
+    "tgemm_debug_build": (ctypes.c_int, []),
     "tgemm_kernel_launches": (ctypes.c_uint64, []),
     "tgemm_version": (ctypes.c_int, []),
 }
@@ -51,19 +56,25 @@ class TgemmError(RuntimeError):
         self.status = status
 
 
+def open_library(path: str):
+    """A ctypes handle on a libtgemm build at ``path`` with every entry point's
+    signature set; raises ImportError if the file does not exist."""
+    if not os.path.exists(path):
+        raise ImportError(f"{os.path.basename(path)} not found at {path}; run dense_tiled_matrix_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
 def load(path: str = LIB_PATH):
     """The loaded library (ctypes.CDLL); raises ImportError if it is not built."""
     global _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(path):
-                raise ImportError(f"libtgemm.so not found at {path}; run dense_tiled_matrix_gb300.build.build()")
-            lib = ctypes.CDLL(path)
-            for name, (res, args) in SIGNATURES.items():
-                fn = getattr(lib, name)
-                fn.restype = res
-                fn.argtypes = args
-            _lib = lib
+            _lib = open_library(path)
         return _lib
 
 
@@ -90,7 +101,7 @@ def _ld(t) -> int:
     return int(t.stride(0))
 
 
-def _call(name, A, B, C, stream, in_dtype):
+def _call(name, A, B, C, stream, in_dtype, lib=None):
     import torch
     if A.dtype != in_dtype or B.dtype != in_dtype:
         raise TypeError(f"{name}: inputs must be {in_dtype}")
@@ -105,35 +116,37 @@ def _call(name, A, B, C, stream, in_dtype):
     for t in (A, B, C):
         if t.numel() and not t.is_cuda:
             raise ValueError(f"{name}: tensors must live on a CUDA device")
-    fn = getattr(load(), name)
-    _check(fn(m, n, k, A.data_ptr() or None, _ld(A), B.data_ptr() or None, _ld(B),
-              C.data_ptr() or None, _ld(C), _stream_handle(stream)))
+    lib = lib or load()
+    status = getattr(lib, name)(m, n, k, A.data_ptr() or None, _ld(A), B.data_ptr() or None, _ld(B),
+                                C.data_ptr() or None, _ld(C), _stream_handle(stream))
+    if status != TGEMM_OK:
+        raise TgemmError(status, f"{lib.tgemm_status_string(status).decode()}: {lib.tgemm_last_error().decode()}")
     return C
 
 
-def tgemm_f32(A, B, C=None, stream=None):
+def tgemm_f32(A, B, C=None, stream=None, lib=None):
     """C = A @ B for float32 tensors on the FMA pipes (fp32 throughout)."""
     import torch
-    return _call("tgemm_f32", A, B, C, stream, torch.float32)
+    return _call("tgemm_f32", A, B, C, stream, torch.float32, lib)
 
 
-def tgemm_tf32(A, B, C=None, stream=None):
+def tgemm_tf32(A, B, C=None, stream=None, lib=None):
     """C = A @ B for float32 tensors on the tensor cores as TF32, fp32 accumulation."""
     import torch
-    return _call("tgemm_tf32", A, B, C, stream, torch.float32)
+    return _call("tgemm_tf32", A, B, C, stream, torch.float32, lib)
 
 
-def tgemm_bf16(A, B, C=None, stream=None):
+def tgemm_bf16(A, B, C=None, stream=None, lib=None):
     """C (float32) = A @ B for bfloat16 tensors on the tensor cores, fp32 accumulation."""
     import torch
-    return _call("tgemm_bf16", A, B, C, stream, torch.bfloat16)
+    return _call("tgemm_bf16", A, B, C, stream, torch.bfloat16, lib)
 
 
-def tgemm_tf32_noalloc(A, B, C=None, stream=None):
+def tgemm_tf32_noalloc(A, B, C=None, stream=None, lib=None):
     """Like ``tgemm_tf32`` but with its scratch in the library's static device
     array (no allocation by the library); the shape must fit TGEMM_NOALLOC_SCRATCH_BYTES."""
     import torch
-    return _call("tgemm_tf32_noalloc", A, B, C, stream, torch.float32)
+    return _call("tgemm_tf32_noalloc", A, B, C, stream, torch.float32, lib)
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -170,6 +183,15 @@ def tgemm_get_device_status(stream=None) -> int:
 def tgemm_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
     """Queues a kernel whose bounded wait must time out after ``limit_ns``; returns the call status."""
     return int(load().tgemm_selftest_wait_timeout(int(limit_ns), _stream_handle(stream)))
+
+
+def tgemm_selftest_debug_check(stream=None) -> int:
+    """Queues a kernel that records a failed device check; returns the call status."""
+    return int(load().tgemm_selftest_debug_check(_stream_handle(stream)))
+
+
+def tgemm_debug_build() -> int:
+    return int(load().tgemm_debug_build())
 
 
 def tgemm_kernel_launches() -> int:

@@ -74,7 +74,12 @@ typedef enum tgemm_status {
     /* A kernel gave up on a pipeline wait after its time limit. */
     TGEMM_ERR_TIMEOUT = 5,
     /* Temporary workspace could not be allocated. */
-    TGEMM_ERR_WORKSPACE = 6
+    TGEMM_ERR_WORKSPACE = 6,
+    /* A device-side consistency check failed: an index outside its buffer or
+     * a pipeline wait that found the wrong phase.  Only the debug build
+     * (libtgemm_debug.so, compiled with TGEMM_DEBUG) carries these checks;
+     * tgemm_get_device_status() reports the file and line. */
+    TGEMM_ERR_INTERNAL = 7
 } tgemm_status;
 
 /*
@@ -177,7 +182,8 @@ const char *tgemm_last_error(void);
 
 /* Waits for `stream`, then reads and clears the current device's status word.
  * Returns TGEMM_OK, TGEMM_ERR_TIMEOUT if a kernel gave up on a wait since the
- * last read, or TGEMM_ERR_CUDA if the synchronisation itself failed. */
+ * last read, TGEMM_ERR_INTERNAL if a device-side check of the debug build
+ * failed, or TGEMM_ERR_CUDA if the synchronisation itself failed. */
 tgemm_status tgemm_get_device_status(struct CUstream_st *stream);
 
 /* Test of the failure path (the pages have no counterpart).  Queues on
@@ -189,6 +195,18 @@ tgemm_status tgemm_get_device_status(struct CUstream_st *stream);
  * CUDA context stays usable.  Returns TGEMM_OK once the kernel is queued,
  * TGEMM_ERR_INVALID_VALUE for a limit outside the range. */
 tgemm_status tgemm_selftest_wait_timeout(int64_t limit_ns, struct CUstream_st *stream);
+
+/* Test of the debug checks' reporting path (the pages have no counterpart).
+ * Queues on `stream` a one-thread kernel that records a failed consistency
+ * check in the device status word, exactly as a failing check of the debug
+ * build does, and returns; it touches no other memory.  A following
+ * tgemm_get_device_status() must report TGEMM_ERR_INTERNAL with the check's
+ * file and line.  Available in every build. */
+tgemm_status tgemm_selftest_debug_check(struct CUstream_st *stream);
+
+/* 1 if this library was built with the device-side consistency checks
+ * (libtgemm_debug.so), else 0. */
+int tgemm_debug_build(void);
 
 /* Kernels launched by this library in this process so far (all devices). */
 uint64_t tgemm_kernel_launches(void);
