@@ -58,6 +58,84 @@ struct SkinnyCfg {
     static_assert(NT * NM * kTileN * 4 <= STAGES * STAGE_B, "partial sums must fit in the B stages");
 };
 
+// The end of a skinny CTA: its 128 x NM partial sums (tensor memory, read by
+// warps 0-3, warp w holding columns n0 + 128t + 32w + lane) go to its own
+// shared memory, the cluster synchronises, CTA r adds rows r, r + S, ... of
+// all S partials in rank order 0..S-1 through distributed shared memory
+// (threads 0-127, one column each) and stores them, and a second cluster
+// barrier keeps the partials alive until every CTA has read them.  Every
+// thread of the CTA calls this.
+template <int NM, int NT>
+__device__ __forceinline__ void cluster_sum_and_store(uint32_t tmem, float* red, bool have, uint64_t* done,
+                                                      int n0, int M, int N, float* __restrict__ C, int64_t ldc,
+                                                      uint32_t* status) {
+    using G = SkinnyCfg<NM, NT>;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_cta_rank();
+    const uint32_t splits = gridDim.y;
+    __syncwarp();
+    if (warp < 4) {
+        if (have && !mbar_wait(done, 0, status)) have = false;
+        tc_fence_after_sync();
+        __syncwarp();   // tcgen05.ld is warp-collective
+        const int jrow = warp * 32 + lane;   // tensor-memory lane = column n0 + 128t + jrow of C
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + t * G::COLS;
+            float* red_t = red + t * NM * kTileN;
+            if (NM == 16) {
+                uint32_t r[16];
+                tmem_load_16(taddr, r);
+                tmem_load_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) red_t[j * kTileN + jrow] = have ? __uint_as_float(r[j]) : 0.0f;
+            } else {
+#pragma unroll
+                for (int c = 0; c < NM / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_load_32(taddr + c * 32, r);
+                    tmem_load_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        red_t[(c * 32 + j) * kTileN + jrow] = have ? __uint_as_float(r[j]) : 0.0f;
+                }
+            }
+        }
+        tc_fence_before_sync();
+    }
+    __syncwarp();
+    cluster_sync_all();
+
+    // --------------------------- add the S partials in rank order, store --
+    const int rows = M < NM ? M : NM;
+    const uint32_t my_red = smem_addr(red);
+    // every rank of the cluster exists and fits the rank-order sum
+    (void)TGEMM_DCHECK(splits <= kMaxSplit && rank < splits, status, kFileSkinny);
+    if (threadIdx.x < kTileN) {
+        for (int item = static_cast<int>(rank); item < NT * rows; item += static_cast<int>(splits)) {
+            const int t = item / rows, mr = item - t * rows;
+            const int n = n0 + t * kTileN + static_cast<int>(threadIdx.x);
+            const uint32_t off =
+                static_cast<uint32_t>(((t * NM + mr) * kTileN + static_cast<int>(threadIdx.x)) * 4);
+            // the partial sum read lies inside the B stages that hold the partials
+            if (!TGEMM_DCHECK(off + 4 <= G::STAGES * G::STAGE_B, status, kFileSkinny)) continue;
+            // all remote loads first (they overlap), then the sum in rank order
+            float part[kMaxSplit];
+#pragma unroll
+            for (int q = 0; q < kMaxSplit; ++q)
+                part[q] = q < static_cast<int>(splits) ? ld_cluster_f32(cluster_map(my_red + off, q)) : 0.0f;
+            float sum = 0.0f;
+#pragma unroll
+            for (int q = 0; q < kMaxSplit; ++q)
+                if (q < static_cast<int>(splits)) sum += part[q];
+            if (n < N) C[static_cast<int64_t>(mr) * ldc + n] = sum;
+        }
+    }
+    __syncwarp();
+    cluster_sync_all();   // partials stay readable until every CTA is done with them
+}
+
 template <int NM, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
 umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -83,7 +161,6 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = cluster_cta_rank();
-    const uint32_t splits = gridDim.y;
     const int n0 = blockIdx.x * kTileN * NT;
     const int KT = (K + kBK - 1) / kBK;
     const int kb0 = static_cast<int>(rank) * kb_per_split;
@@ -179,64 +256,7 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         if (last_s >= 0) mbar_wait(&empty[last_s], last_ph, status, kDrainLimitNs);
     }
 
-    // ------------------------------------- partial sums -> shared memory --
-    __syncwarp();
-    bool have = nkb > 0;
-    if (have && !mbar_wait(done, 0, status)) have = false;
-    tc_fence_after_sync();
-    __syncwarp();   // tcgen05.ld is warp-collective
-    const int jrow = warp * 32 + lane;   // tensor-memory lane = column n0 + 128t + jrow of C
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + t * G::COLS;
-        float* red_t = red + t * NM * kTileN;
-        if (NM == 16) {
-            uint32_t r[16];
-            tmem_load_16(taddr, r);
-            tmem_load_wait();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) red_t[j * kTileN + jrow] = have ? __uint_as_float(r[j]) : 0.0f;
-        } else {
-#pragma unroll
-            for (int c = 0; c < NM / 32; ++c) {
-                uint32_t r[32];
-                tmem_load_32(taddr + c * 32, r);
-                tmem_load_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    red_t[(c * 32 + j) * kTileN + jrow] = have ? __uint_as_float(r[j]) : 0.0f;
-            }
-        }
-    }
-    tc_fence_before_sync();
-    __syncwarp();
-    cluster_sync_all();
-
-    // --------------------------- add the S partials in rank order, store --
-    const int rows = M < NM ? M : NM;
-    const uint32_t my_red = smem_addr(red);
-    // every rank of the cluster exists and fits the rank-order sum
-    (void)TGEMM_DCHECK(splits <= kMaxSplit && rank < splits, status, kFileSkinny);
-    for (int item = static_cast<int>(rank); item < NT * rows; item += static_cast<int>(splits)) {
-        const int t = item / rows, mr = item - t * rows;
-        const int n = n0 + t * kTileN + static_cast<int>(threadIdx.x);
-        const uint32_t off =
-            static_cast<uint32_t>(((t * NM + mr) * kTileN + static_cast<int>(threadIdx.x)) * 4);
-        // the partial sum read lies inside the B stages that hold the partials
-        if (!TGEMM_DCHECK(off + 4 <= G::STAGES * G::STAGE_B, status, kFileSkinny)) continue;
-        // all remote loads first (they overlap), then the sum in rank order
-        float part[kMaxSplit];
-#pragma unroll
-        for (int q = 0; q < kMaxSplit; ++q)
-            part[q] = q < static_cast<int>(splits) ? ld_cluster_f32(cluster_map(my_red + off, q)) : 0.0f;
-        float sum = 0.0f;
-#pragma unroll
-        for (int q = 0; q < kMaxSplit; ++q)
-            if (q < static_cast<int>(splits)) sum += part[q];
-        if (n < N) C[static_cast<int64_t>(mr) * ldc + n] = sum;
-    }
-    __syncwarp();
-    cluster_sync_all();   // partials stay readable until every CTA is done with them
+    cluster_sum_and_store<NM, NT>(tmem, red, nkb > 0, done, n0, M, N, C, ldc, status);
 
     if (warp == 1) {   // the allocating warp frees the tensor memory
         __syncwarp();
@@ -244,6 +264,20 @@ umma_skinny_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         tmem_dealloc(tmem, G::TMEM_COLS);
     }
     (void)ok;
+}
+
+// Split of k over the CTAs of a cluster: about 5/3 CTAs per SM, at most
+// kMaxSplit, no empty slice.
+void skinny_split(const Problem& p, const Device& dev, int tiles, int* splits_out, int* kb_per_split_out) {
+    const int KT = (p.k + kBK - 1) / kBK;
+    const int target = kTargetCtasPer3Sms * dev.sm_count / 3;
+    int splits = (target + tiles / 2) / tiles;
+    splits = splits < 1 ? 1 : splits;
+    splits = splits > kMaxSplit ? kMaxSplit : splits;
+    splits = splits > KT ? KT : splits;
+    const int kb_per_split = (KT + splits - 1) / splits;
+    *splits_out = (KT + kb_per_split - 1) / kb_per_split;
+    *kb_per_split_out = kb_per_split;
 }
 
 template <int NM>
@@ -264,14 +298,8 @@ cudaError_t launch_nm(const Problem& p, const Device& dev) {
         return err;
     }
     const int tiles = (p.n + kTileN * NT - 1) / (kTileN * NT);
-    const int KT = (p.k + kBK - 1) / kBK;
-    const int target = kTargetCtasPer3Sms * dev.sm_count / 3;
-    int splits = (target + tiles / 2) / tiles;
-    splits = splits < 1 ? 1 : splits;
-    splits = splits > kMaxSplit ? kMaxSplit : splits;
-    splits = splits > KT ? KT : splits;
-    const int kb_per_split = (KT + splits - 1) / splits;
-    splits = (KT + kb_per_split - 1) / kb_per_split;   // no empty slices
+    int splits = 1, kb_per_split = 1;
+    skinny_split(p, dev, tiles, &splits, &kb_per_split);
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(tiles), static_cast<unsigned>(splits), 1);
