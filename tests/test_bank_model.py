@@ -197,3 +197,50 @@ def test_transpose_strips_cover_the_tile_once():
                     assert (r, 4 * j + e) not in seen
                     seen.add((r, 4 * j + e))
     assert seen == {(r, c) for r in range(128) for c in range(32)}
+
+
+# ---- tensor-core epilogue (csrc/umma.cu): per-warp 32 x 32 fp32 staging tile ----
+# Lane l holds row l of a 32 x 32 block (one tcgen05.ld); 16-byte chunk q of
+# row i is stored at chunk q ^ (i % 8).
+
+def epi_offset(row, chunk, word=0):
+    return row * 128 + ((chunk ^ (row & 7)) << 4) + 4 * word
+
+
+def test_epilogue_tile_writes_one_pass_per_quarter_warp():
+    # float4 store of chunk q by every lane: lane l writes row l
+    for q in range(8):
+        for quarter in range(4):
+            addrs = [epi_offset(l, q) for l in range(8 * quarter, 8 * quarter + 8)]
+            assert wavefronts(addrs, width=16) == 1, (q, quarter)
+
+
+def test_epilogue_tile_vector_reads_one_pass_per_quarter_warp():
+    # float4 read i: lane reads row 4 i + lane / 8, chunk lane % 8
+    for i in range(8):
+        for quarter in range(4):
+            lanes = range(8 * quarter, 8 * quarter + 8)
+            addrs = [epi_offset(4 * i + (l >> 3), l & 7) for l in lanes]
+            assert wavefronts(addrs, width=16) == 1, (i, quarter)
+
+
+def test_epilogue_tile_scalar_reads_one_pass():
+    # unaligned C: the warp reads one row, lane l takes word l (chunk l / 4, word l % 4)
+    for rr in range(32):
+        addrs = [epi_offset(rr, l >> 2, l & 3) for l in range(32)]
+        assert wavefronts(addrs) == 1, rr
+
+
+def test_epilogue_tile_would_conflict_without_the_swizzle():
+    plain = lambda row, chunk: row * 128 + (chunk << 4)
+    # the row-wise writes of one chunk by 8 rows land in one bank group: 8 passes
+    assert wavefronts([plain(l, 3) for l in range(8)], width=16) == 8
+
+
+def test_epilogue_tile_reads_cover_the_block_once():
+    seen = set()
+    for i in range(8):
+        for l in range(32):
+            rr, q = 4 * i + (l >> 3), l & 7
+            seen.add((rr, q))
+    assert seen == {(r, q) for r in range(32) for q in range(8)}
