@@ -521,6 +521,37 @@ def bench_tgemm(args, world, rank, local):
                     "frac_of_hbm": round(gbs / float(peaks["hbm_gbs"]), 4)}
             del srcs, dst
 
+    # Read-stream ceilings (libtgemm_probes): 128 MiB -- the skinny product's B --
+    # read once through TMA bulk copies and once with 128-bit loads, four
+    # rotated buffers (512 MiB, about 4x L2); the skinny kernel's bandwidth is
+    # reported as a fraction of each beside its fraction of the copy peak.
+    read_streams = {}
+    if extras and not only:
+        from dense_tiled_matrix_gb300 import probes
+        nbytes = 128 * 2 ** 20
+        bufs = [torch.randint(-2 ** 31, 2 ** 31 - 1, (nbytes // 4,), dtype=torch.int32, device=dev)
+                for _ in range(4)]
+        total = torch.zeros(1, dtype=torch.int64, device=dev)
+        for how in ("tma", "ldg"):
+            ev = []
+            for it in range(args.warmup + 20):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                probes.read_stream(bufs[it % 4], how, total, stream)
+                e1.record(stream)
+                ev.append((e0, e1))
+            torch.cuda.synchronize(dev)
+            med = statistics.median(a.elapsed_time(b) / 1e3 for a, b in ev[args.warmup:])
+            gbs = nbytes / med / 1e9
+            read_streams[how] = {"us": round(med * 1e6, 2), "GB_s": round(gbs, 1),
+                                 "frac_of_hbm": round(gbs / float(peaks["hbm_gbs"]), 4)}
+        del bufs
+        if "skinny_bf16" in parts:
+            sk = parts["skinny_bf16"]["roofline"]["achieved"]
+            for how in read_streams:
+                read_streams[how]["skinny_frac"] = round(sk / read_streams[how]["GB_s"], 4)
+
     # End to end through the C ABI: pinned host inputs -> device, product, result -> host.
     e2e = None
     if not args.no_e2e and runs:
@@ -578,7 +609,8 @@ def bench_tgemm(args, world, rank, local):
                 "scaling": "strong" if shard_rows else "weak", "vs_baseline": None, "dtype": "bf16+f32",
                 "data": "synthetic (seeded SplitMix64; bf16 N(0,1)/sqrt(k), fp32 N(0,1))",
                 "config": step_config(world, shard_rows),
-                "roofline": roof, "parts": parts, "transposes": transposes, "cpu_baseline": cpu, "e2e": e2e,
+                "roofline": roof, "parts": parts, "transposes": transposes, "read_streams": read_streams,
+                "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": int(launches), "clocks": clock_summary,
                 "fp32_peak": {"tflops": round(fp32[0], 2), "derivation": fp32[1]},
                 "wall_s_timed_region": round(t_wall, 3), "impl": "tgemm"}

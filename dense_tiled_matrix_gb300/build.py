@@ -22,6 +22,8 @@ LIB_PATH = os.path.join(PKG, "libtgemm.so")
 DEBUG_LIB_PATH = os.path.join(PKG, "libtgemm_debug.so")   # with the device-side checks (TGEMM_DEBUG)
 PAGES_DIR = os.path.join(PKG, "csrc_pages")
 PAGES_LIB_PATH = os.path.join(PKG, "libtgemm_pages.so")
+PROBES_DIR = os.path.join(PKG, "csrc_probes")
+PROBES_LIB_PATH = os.path.join(PKG, "libtgemm_probes.so")   # read-stream calibration (include/tgemm_probes.h)
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
@@ -95,15 +97,19 @@ def _build_lib(srcs, lib_path, tag, verbose, force, ptxas_verbose, extra=()):
 
 def build(verbose: bool = False, force: bool = False, ptxas_verbose: bool = False) -> str:
     """Compile and link ``libtgemm.so``, its debug build ``libtgemm_debug.so``
-    (the same sources with the device-side consistency checks, TGEMM_DEBUG) and
-    the pages' comparator library; returns libtgemm's path."""
-    with ThreadPoolExecutor(max_workers=3) as pool:
+    (the same sources with the device-side consistency checks, TGEMM_DEBUG), the
+    pages' comparator library and the read-stream calibration library; returns
+    libtgemm's path."""
+    with ThreadPoolExecutor(max_workers=4) as pool:
         main = pool.submit(_build_lib, sources(), LIB_PATH, "tgemm", verbose, force, ptxas_verbose)
         debug = pool.submit(_build_lib, sources(), DEBUG_LIB_PATH, "tgemm_dbg", verbose, force, ptxas_verbose,
                             ("-DTGEMM_DEBUG",))
         pages = pool.submit(_build_lib, sources(PAGES_DIR), PAGES_LIB_PATH, "pages", verbose, force,
                             ptxas_verbose)
+        probes = pool.submit(_build_lib, sources(PROBES_DIR), PROBES_LIB_PATH, "probes", verbose, force,
+                             ptxas_verbose)
         pages.result()
+        probes.result()
         debug.result()
         return main.result()
 

@@ -7,11 +7,12 @@ import re
 import pytest
 
 from dense_tiled_matrix_gb300 import build as tbuild
-from dense_tiled_matrix_gb300 import pages, tgemm
+from dense_tiled_matrix_gb300 import pages, probes, tgemm
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "tgemm.h")
 PAGES_HEADER = os.path.join(ROOT, "include", "tgemm_pages.h")
+PROBES_HEADER = os.path.join(ROOT, "include", "tgemm_probes.h")
 
 
 @pytest.fixture(scope="module")
@@ -28,7 +29,22 @@ def declared_functions(header=HEADER):
 
 def test_every_header_under_include_is_checked():
     headers = sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
-    assert headers == ["tgemm.h", "tgemm_pages.h"]
+    assert headers == ["tgemm.h", "tgemm_pages.h", "tgemm_probes.h"]
+
+
+def test_probes_library_exports_its_header_and_checks_arguments():
+    tbuild.build()
+    lib = probes.load()
+    names = declared_functions(PROBES_HEADER)
+    assert names == sorted(probes.SIGNATURES)
+    fake_buf, fake_sum = 0x10000000, 0x20000000
+    for name in names:
+        fn = getattr(lib, name)
+        assert fn(fake_buf, 17, fake_sum, None) == 1          # not a multiple of 16 bytes
+        assert fn(fake_buf + 8, 32, fake_sum, None) == 1      # buffer not 16-byte aligned
+        assert fn(fake_buf, 32, None, None) == 1              # no sum
+        assert fn(fake_buf, -16, fake_sum, None) == 1
+        assert fn(None, 0, fake_sum, None) == 0               # empty: nothing queued
 
 
 def test_pages_library_exports_its_header():
@@ -65,7 +81,7 @@ def test_every_declared_symbol_is_exported_and_bound(lib):
 
 
 def test_status_strings_and_version(lib):
-    for code in range(7):
+    for code in range(8):
         text = tgemm.tgemm_status_string(code)
         assert text and text != "unknown status"
     assert tgemm.tgemm_status_string(99) == "unknown status"
