@@ -16,7 +16,9 @@ The same JSON line carries, for information, the other measured shapes
 (4096^3 on the TF32 tensor-core path, 16 x 8192 x 8192 bf16, the
 4097 x 3001 x 1023 fp32 edge-tile case), a roofline object for the kernel
 taking most of the step's time, the end-to-end number through the C ABI from
-pinned host buffers, the CPU oracle timed on a bounded sample of the same
+pinned host buffers (every step copies its inputs in and its results out; the
+copies run on their own streams beside the products, and the same step with
+nothing overlapped is reported with it), the CPU oracle timed on a bounded sample of the same
 workload, and the SM clocks sampled while timing.  After the timed region each
 shape is also launched back to back between a single event pair
 (``ms_back_to_back``): the per-launch event pairs add a microsecond or two,
@@ -552,7 +554,13 @@ def bench_tgemm(args, world, rank, local):
             for how in read_streams:
                 read_streams[how]["skinny_frac"] = round(sk / read_streams[how]["GB_s"], 4)
 
-    # End to end through the C ABI: pinned host inputs -> device, product, result -> host.
+    # End to end through the C ABI: pinned host inputs -> device, product, result -> host,
+    # every step.  The copies run as a pipeline beside the products: inputs go in on
+    # a copy stream, the products run on the compute stream as each part's inputs
+    # land, results come back on a third stream as each product finishes, and two
+    # sets of device buffers alternate between steps so that step i + 1's inputs
+    # can land while step i computes and reads back (each set is reused only after
+    # the products and the read-back that used it two steps before are done).
     e2e = None
     if not args.no_e2e and runs:
         host = {}
@@ -564,34 +572,86 @@ def bench_tgemm(args, world, rank, local):
             hA.copy_(A)
             hB.copy_(B)
             hC = torch.empty(C.shape, dtype=C.dtype, pin_memory=True)
-            dA, dB, dC = torch.empty_like(A), torch.empty_like(B), torch.empty_like(C)
-            host[name] = (hA, hB, hC, dA, dB, dC, runs[name][3])
+            sets = [(torch.empty_like(A), torch.empty_like(B), torch.empty_like(C)) for _ in range(2)]
+            host[name] = (hA, hB, hC, sets, runs[name][3])
             h2d += hA.numel() * hA.element_size() + hB.numel() * hB.element_size()
             d2h += hC.numel() * hC.element_size()
+        s_in = torch.cuda.Stream(dev)
+        s_out = torch.cuda.Stream(dev)
+        freed = [None, None]   # per buffer set: the event after which it may be overwritten
 
-        def e2e_step():
-            for hA, hB, hC, dA, dB, dC, fn in host.values():
+        def e2e_step(i):
+            b = i % 2
+            landed, done = {}, {}
+            if freed[b] is not None:
+                s_in.wait_event(freed[b])
+            for name, (hA, hB, hC, sets, fn) in host.items():
+                dA, dB, _ = sets[b]
+                with torch.cuda.stream(s_in):
+                    dA.copy_(hA, non_blocking=True)
+                    dB.copy_(hB, non_blocking=True)
+                landed[name] = torch.cuda.Event()
+                landed[name].record(s_in)
+            if freed[b] is not None:
+                stream.wait_event(freed[b])
+            for name, (hA, hB, hC, sets, fn) in host.items():
+                dA, dB, dC = sets[b]
+                stream.wait_event(landed[name])
+                fn(dA, dB, dC, stream)
+                done[name] = torch.cuda.Event()
+                done[name].record(stream)
+            for name, (hA, hB, hC, sets, fn) in host.items():
+                s_out.wait_event(done[name])
+                with torch.cuda.stream(s_out):
+                    hC.copy_(sets[b][2], non_blocking=True)
+            freed[b] = torch.cuda.Event()
+            freed[b].record(s_out)
+
+        for i in range(args.warmup):
+            e2e_step(i)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        freed[0] = freed[1] = None
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        s_in.wait_event(e0)
+        for i in range(args.steps):
+            e2e_step(i)
+        stream.wait_event(freed[(args.steps - 1) % 2])
+        if args.steps > 1:
+            stream.wait_event(freed[args.steps % 2])
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps, world)
+
+        # The same step with nothing overlapped (copies, products and read-back one
+        # after another on one stream), for comparison.
+        def serial_step():
+            for hA, hB, hC, sets, fn in host.values():
+                dA, dB, dC = sets[0]
                 dA.copy_(hA, non_blocking=True)
                 dB.copy_(hB, non_blocking=True)
                 fn(dA, dB, dC, stream)
                 hC.copy_(dC, non_blocking=True)
 
-        for _ in range(args.warmup):
-            e2e_step()
+        serial_step()
         torch.cuda.synchronize(dev)
         barrier(world)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(args.steps):
-            e2e_step()
+            serial_step()
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps, world)
-        e2e_value = flops_step / e2e_s / 1e12 if shard_rows else world * flops_step / e2e_s / 1e12
-        e2e = {"value": round(e2e_value, 3), "unit": UNIT,
+        serial_s = max_over_ranks(e0.elapsed_time(e1) / 1e3 / args.steps, world)
+        scale = 1 if shard_rows else world
+        e2e = {"value": round(scale * flops_step / e2e_s / 1e12, 3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": round(e2e_s * 1e3, 3)}
+               "ms_per_step": round(e2e_s * 1e3, 3),
+               "how": "input copies, products and read-back pipelined on three streams, two buffer sets",
+               "serial": {"value": round(scale * flops_step / serial_s / 1e12, 3),
+                          "ms_per_step": round(serial_s * 1e3, 3),
+                          "how": "the same copies and products one after another on one stream"}}
 
     status = tgemm.tgemm_get_device_status(stream)
     if status != tgemm.TGEMM_OK:
