@@ -272,3 +272,44 @@ def test_large_single_extent(mode, shape):
     m, n, k = shape
     parity.full_check(mode, inputs.random_case(7000 + m % 997 + 7 * (n % 991) + 13 * k, m, n, k, kind="int"),
                       f"{mode} int {shape}")
+
+
+def _strided_cases(count, seed):
+    """Seeded shapes, each operand a view into a larger buffer: a random row
+    padding (leading dimension = extent + 0..9) and a random base offset of
+    0..3 elements, so every combination of 16-byte-aligned and misaligned
+    operands and C appears (re-pitch, vector and scalar epilogue stores)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        m, n, k = (int(x) for x in rng.integers(1, 700, 3))
+        pads = tuple(int(x) for x in rng.integers(0, 10, 3))
+        offs = tuple(int(x) for x in rng.integers(0, 4, 3))
+        out.append((m, n, k, pads, offs))
+    return out
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("case_spec", _strided_cases(12, 4711), ids=lambda c: "x".join(map(str, c[:3])))
+def test_random_views_exact_and_nothing_written_outside_c(mode, case_spec):
+    m, n, k, (pa, pb, pc), (oa, ob, oc) = case_spec
+    case = inputs.random_case(17 * m + 5 * n + k, m, n, k, kind="int")
+    A_np, B_np = parity.inputs_for(mode, case)
+    dtype = torch.bfloat16 if mode == "bf16" else torch.float32
+    A_buf = torch.zeros(oa + m * (k + pa), dtype=dtype, device="cuda")
+    B_buf = torch.zeros(ob + k * (n + pb), dtype=dtype, device="cuda")
+    C_buf = torch.full((oc + m * (n + pc) + 8,), float("nan"), device="cuda")
+    A = A_buf[oa:oa + m * (k + pa)].view(m, k + pa)[:, :k]
+    B = B_buf[ob:ob + k * (n + pb)].view(k, n + pb)[:, :n]
+    C = C_buf[oc:oc + m * (n + pc)].view(m, n + pc)[:, :n]
+    A.copy_(parity.to_device(A_np))
+    B.copy_(parity.to_device(B_np))
+    parity.ENTRY[mode](A, B, C)
+    torch.cuda.synchronize()
+    P, D = oracle.gemm(A_np, B_np)
+    parity.check(mode, C.cpu().numpy(), P, D, True, f"{mode} view {case_spec}")
+    host = C_buf.cpu().numpy()
+    inside = np.zeros(host.shape, dtype=bool)
+    for i in range(m):
+        inside[oc + i * (n + pc): oc + i * (n + pc) + n] = True
+    assert np.all(np.isnan(host[~inside])), "wrote outside C"
