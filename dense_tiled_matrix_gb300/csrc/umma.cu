@@ -29,7 +29,7 @@
 //    overlap the MMAs of the next.
 //  * Warps 2-5 drain an accumulator with tcgen05.ld (warp w reads lanes
 //    32*(w%4) .. +31, i.e. 32 rows of C, one row per lane), turn each 32 x 32
-//    block through a swizzled shared tile so that a warp store covers whole
+//    block through a padded shared tile so that a warp store covers whole
 //    128-byte row segments of C (128-bit stores where C's rows are 16-byte
 //    aligned), masked at the edges of C.
 //
@@ -68,8 +68,10 @@ struct Cfg {
     static constexpr int GROUP_M = kWide ? 8 : 16;
     static constexpr uint32_t IDESC =
         instr_desc(kTF32 ? kFormatTF32 : kFormatBF16, 0, kBKMajor ? 0u : 1u, 128, BN);
-    // per epilogue warp a 32 x 32 fp32 tile that turns TMEM rows into coalesced row segments of C
-    static constexpr uint32_t EPI_BYTES = 4 * 32 * 32 * 4;
+    // per epilogue warp a 32 x 32 fp32 tile, rows padded to 36 floats, that turns
+    // TMEM rows into coalesced row segments of C
+    static constexpr int EPI_PITCH = 36;
+    static constexpr uint32_t EPI_BYTES = 4 * 32 * EPI_PITCH * 4;
     static constexpr size_t SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + EPI_BYTES + (2 * STAGES + 4) * 8 + 16;
     static_assert(ACCS * HALVES * 256 <= 512, "accumulators exceed tensor memory");
     static_assert(BN % 32 == 0 && BN <= 256, "tile width");
@@ -110,7 +112,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     uint8_t* smem = smem_align_1024(smem_raw);
     uint8_t* sA = smem;
     uint8_t* sB = smem + G::STAGES * G::A_BYTES;
-    float* sEpi = reinterpret_cast<float*>(sB + G::STAGES * G::B_BYTES);   // 4 x 32 x 32 fp32
+    float* sEpi = reinterpret_cast<float*>(sB + G::STAGES * G::B_BYTES);   // 4 x 32 x 36 fp32
     uint64_t* full = reinterpret_cast<uint64_t*>(sB + G::STAGES * G::B_BYTES + G::EPI_BYTES);
     uint64_t* empty = full + G::STAGES;
     uint64_t* acc_full = empty + G::STAGES;    // [2]
@@ -287,7 +289,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // waiting at a named barrier.
         const int quarter = warp & 3;   // tensor-memory lanes 32*quarter .. +31
         const int row_in_half = quarter * 32 + lane;
-        float* epi = sEpi + (warp - 2) * 32 * 32;   // this warp's 32 x 32 staging tile
+        float* epi = sEpi + (warp - 2) * 32 * G::EPI_PITCH;   // this warp's 32 x 32 staging tile
         bool ok = true;
         int it = 0;
         Seq sq;
@@ -353,11 +355,14 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     // transpose case study): lane l holds row l of this 32 x 32 block;
                     // through the warp's shared tile the warp then writes whole row
                     // segments, 128 contiguous bytes per row, instead of 32 rows at once.
-                    // 16-byte chunk q of tile row i sits at chunk q ^ (i % 8), so the
-                    // row-wise writes and the column-wise reads are conflict-free.
+                    // Tile rows are 36 floats apart, so the 8 lanes of a quarter warp
+                    // storing 16-byte chunk q of 8 consecutive rows hit 8 different
+                    // bank groups, and a row read back is 128 contiguous bytes.  (An
+                    // XOR-swizzled 32-float row is conflict-free as well, but measured
+                    // slower where C's rows are not 16-byte aligned.)
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
-                        *reinterpret_cast<float4*>(epi + lane * 32 + ((q ^ (lane & 7)) << 2)) =
+                        *reinterpret_cast<float4*>(epi + lane * G::EPI_PITCH + 4 * q) =
                             make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
                                         __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
                     __syncwarp();
@@ -370,7 +375,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const int rr = 4 * i + (lane >> 3);
-                            const float4 v = *reinterpret_cast<const float4*>(epi + rr * 32 + ((q ^ (rr & 7)) << 2));
+                            const float4 v = *reinterpret_cast<const float4*>(epi + rr * G::EPI_PITCH + 4 * q);
                             if (row0 + rr < M) {
                                 float* dst = C + static_cast<int64_t>(row0 + rr) * ldc + col;
                                 if (col + 4 <= N) {
@@ -389,7 +394,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         const int q = lane >> 2, w = lane & 3;
 #pragma unroll 8
                         for (int rr = 0; rr < 32; ++rr) {
-                            const float v = epi[rr * 32 + ((q ^ (rr & 7)) << 2) + w];
+                            const float v = epi[rr * G::EPI_PITCH + 4 * q + w];
                             if (row0 + rr < M && col < N) C[static_cast<int64_t>(row0 + rr) * ldc + col] = v;
                         }
                     }

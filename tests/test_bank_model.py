@@ -16,9 +16,15 @@ own count for a 128-bit load, ncu's wavefronts, is at least 2 -- 2 for the A
 reads, 4 for the B reads on GB300 -- and bank conflicts would add to it); the
 TMA 64-byte swizzle it relies on is
 checked against the kernel's own chunk formula.  So are the TMA transpose's
-reads of a 128-byte-swizzled input tile and its writes of the output tile.
+reads of a 128-byte-swizzled input tile and its writes of the output tile, and
+the tensor-core epilogue's padded staging tile.
 """
+import os
+import re
+
 import pytest
+
+CSRC = os.path.join(os.path.dirname(os.path.abspath(__file__)), "..", "dense_tiled_matrix_gb300", "csrc")
 
 BANKS = 32
 
@@ -200,11 +206,20 @@ def test_transpose_strips_cover_the_tile_once():
 
 
 # ---- tensor-core epilogue (csrc/umma.cu): per-warp 32 x 32 fp32 staging tile ----
-# Lane l holds row l of a 32 x 32 block (one tcgen05.ld); 16-byte chunk q of
-# row i is stored at chunk q ^ (i % 8).
+# Lane l holds row l of a 32 x 32 block (one tcgen05.ld); tile rows are padded
+# to 36 floats (144 bytes), 16-byte chunk q of row i at byte 144 i + 16 q.
+EPI_PITCH = 36
+
 
 def epi_offset(row, chunk, word=0):
-    return row * 128 + ((chunk ^ (row & 7)) << 4) + 4 * word
+    return row * 4 * EPI_PITCH + (chunk << 4) + 4 * word
+
+
+def test_epilogue_pitch_matches_the_kernel():
+    src = open(os.path.join(CSRC, "umma.cu")).read()
+    assert re.search(r"EPI_PITCH\s*=\s*%d\s*;" % EPI_PITCH, src)
+    assert "4 * 32 * EPI_PITCH * 4" in src
+    assert "epi + lane * G::EPI_PITCH + 4 * q" in src
 
 
 def test_epilogue_tile_writes_one_pass_per_quarter_warp():
@@ -231,7 +246,7 @@ def test_epilogue_tile_scalar_reads_one_pass():
         assert wavefronts(addrs) == 1, rr
 
 
-def test_epilogue_tile_would_conflict_without_the_swizzle():
+def test_epilogue_tile_would_conflict_without_the_padding():
     plain = lambda row, chunk: row * 128 + (chunk << 4)
     # the row-wise writes of one chunk by 8 rows land in one bank group: 8 passes
     assert wavefronts([plain(l, 3) for l in range(8)], width=16) == 8
