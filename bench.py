@@ -554,6 +554,37 @@ def bench_tgemm(args, world, rank, local):
             for how in read_streams:
                 read_streams[how]["skinny_frac"] = round(sk / read_streams[how]["GB_s"], 4)
 
+    # Paired-FMA ceiling (libtgemm_probes): the FFMA product's 8 x 8 register-tile
+    # update with register operands only, one CTA per SM of 8 warps (the product
+    # kernel's consumer warps) and of 16; the fp32 products are reported as a
+    # fraction of it beside their fraction of the derived FP32 peak.
+    alu_ceiling = {}
+    if extras and not only:
+        from dense_tiled_matrix_gb300 import probes
+        ab = torch.tensor([2.0 ** -(i % 4) for i in range(8)] + [2.0 ** (j % 3 - 1) for j in range(8)],
+                          dtype=torch.float32, device=dev)
+        out = torch.zeros(1, dtype=torch.float64, device=dev)
+        iters = 16384
+        for warps in (8, 16):
+            ev = []
+            for it in range(args.warmup + 10):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                probes.ffma2(warps, iters, ab, out, stream)
+                e1.record(stream)
+                ev.append((e0, e1))
+            torch.cuda.synchronize(dev)
+            med = statistics.median(a.elapsed_time(b) / 1e3 for a, b in ev[args.warmup:])
+            flops = 128.0 * sm_count * 32 * warps * iters
+            tf = flops / med / 1e12
+            alu_ceiling[f"ffma2_{warps}_warps"] = {"us": round(med * 1e6, 2), "tflops": round(tf, 2),
+                                                   "frac_of_fp32_peak": round(tf / fp32[0], 4)}
+        best = max(v["tflops"] for v in alu_ceiling.values())
+        for name in ("f32_4096", "irregular_f32", "f32_1024"):
+            if name in parts:
+                alu_ceiling[f"{name}_frac"] = round(parts[name]["tflops"] / best, 4)
+
     # End to end through the C ABI: pinned host inputs -> device, product, result -> host,
     # every step.  The copies run as a pipeline beside the products: inputs go in on
     # a copy stream, the products run on the compute stream as each part's inputs
@@ -669,7 +700,7 @@ def bench_tgemm(args, world, rank, local):
                 "scaling": "strong" if shard_rows else "weak", "vs_baseline": None, "dtype": "bf16+f32",
                 "data": "synthetic (seeded SplitMix64; bf16 N(0,1)/sqrt(k), fp32 N(0,1))",
                 "config": step_config(world, shard_rows),
-                "roofline": roof, "parts": parts, "transposes": transposes, "read_streams": read_streams,
+                "roofline": roof, "parts": parts, "transposes": transposes, "read_streams": read_streams, "alu_ceiling": alu_ceiling,
                 "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": int(launches), "clocks": clock_summary,
                 "fp32_peak": {"tflops": round(fp32[0], 2), "derivation": fp32[1]},

@@ -1,11 +1,13 @@
-// probes.cu -- read-stream calibration kernels (include/tgemm_probes.h).
+// probes.cu -- calibration kernels (include/tgemm_probes.h).
 //
 // Two ways to stream a buffer from HBM into the SMs, each reading every byte
 // once and adding every 32-bit word into a 64-bit checksum (integer addition,
 // so the result does not depend on the order): bulk copies by the TMA unit
 // into a shared-memory ring, as the skinny product streams B, and 128-bit
 // loads from many threads.  Timed by the caller, they give the two read-stream
-// ceilings the skinny product's bandwidth is compared with.
+// ceilings the skinny product's bandwidth is compared with.  A third kernel
+// runs the FFMA product's register-tile update with no memory operands: the
+// paired-FMA rate its consumer loop is compared with.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -121,6 +123,41 @@ probe_ldg_kernel(const uint4* __restrict__ buf, int64_t nvec, unsigned long long
     block_sum(acc, sum);
 }
 
+// Paired-FMA throughput: each thread keeps the FFMA product kernel's 8 x 8
+// register tile (32 accumulator pairs) and updates it from registers only, 32
+// fma.rn.f32x2 per step, `iters` steps; then adds its 64 accumulators, in
+// double, into *out.  The operands are read from memory, so the compiler can
+// neither fold nor merge the chains.
+constexpr int kFfmaMaxWarps = 16;
+__global__ void __launch_bounds__(kFfmaMaxWarps * 32, 1)
+probe_ffma2_kernel(const float* __restrict__ ab, int64_t iters, double* out) {
+    float a[8];
+    float2 b[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = ab[i];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) b[j] = make_float2(ab[8 + 2 * j], ab[9 + 2 * j]);
+    float2 acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
+#pragma unroll 4
+    for (int64_t it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i][j] = __ffma2_rn(make_float2(a[i], a[i]), b[j], acc[i][j]);
+    }
+    double s = 0.0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s += static_cast<double>(acc[i][j].x) + static_cast<double>(acc[i][j].y);
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_down_sync(0xFFFFFFFFu, s, o);
+    if ((threadIdx.x & 31) == 0) atomicAdd(out, s);
+}
+
 int check(const void* buf, int64_t bytes, const uint64_t* sum, int* sms) {
     if (bytes < 0 || bytes % 16 != 0 || bytes >= (int64_t(1) << 40)) return 1;
     if (bytes > 0 && (!buf || reinterpret_cast<uintptr_t>(buf) % 16 != 0)) return 1;
@@ -157,5 +194,18 @@ extern "C" int tgemm_probe_read_ldg(const void* buf, int64_t bytes, uint64_t* su
     const int64_t grid = want < 4 * sms ? want : 4 * sms;
     probe_ldg_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(
         static_cast<const uint4*>(buf), nvec, reinterpret_cast<unsigned long long*>(sum));
+    return cudaGetLastError() == cudaSuccess ? 0 : 4;
+}
+
+extern "C" int tgemm_probe_ffma2(int warps_per_sm, int64_t iters, const float* ab, double* out,
+                                 struct CUstream_st* stream) {
+    if (warps_per_sm < 1 || warps_per_sm > kFfmaMaxWarps || iters < 0 || iters >= (int64_t(1) << 40)) return 1;
+    if (!ab || reinterpret_cast<uintptr_t>(ab) % 4 != 0 || !out || reinterpret_cast<uintptr_t>(out) % 8 != 0)
+        return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 4;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 4;
+    probe_ffma2_kernel<<<static_cast<unsigned>(sms), static_cast<unsigned>(warps_per_sm * 32), 0, stream>>>(
+        ab, iters, out);
     return cudaGetLastError() == cudaSuccess ? 0 : 4;
 }

@@ -1,5 +1,5 @@
-"""Python binding of libtgemm_probes: read-stream calibration kernels
-(``include/tgemm_probes.h``).  Argument marshalling only."""
+"""Python binding of libtgemm_probes: calibration kernels (read streams, the
+paired-FMA rate; ``include/tgemm_probes.h``).  Argument marshalling only."""
 from __future__ import annotations
 
 import ctypes
@@ -12,6 +12,7 @@ _I64, _VP = ctypes.c_int64, ctypes.c_void_p
 SIGNATURES = {
     "tgemm_probe_read_tma": (ctypes.c_int, [_VP, _I64, _VP, _VP]),
     "tgemm_probe_read_ldg": (ctypes.c_int, [_VP, _I64, _VP, _VP]),
+    "tgemm_probe_ffma2": (ctypes.c_int, [ctypes.c_int, _I64, _VP, _VP, _VP]),
 }
 
 _lock = threading.Lock()
@@ -47,3 +48,20 @@ def read_stream(buf, how: str, sum_out, stream=None) -> None:
     rc = fn(buf.data_ptr() or None, nbytes, sum_out.data_ptr(), int(stream.cuda_stream))
     if rc != 0:
         raise RuntimeError(f"tgemm_probe_read_{how}: status {rc}")
+
+
+def ffma2(warps_per_sm: int, iters: int, ab, out, stream=None) -> None:
+    """Queue the paired-FMA probe: ``ab`` a 16-element float32 CUDA tensor
+    (a[0..7], b[0..7]), ``out`` a 1-element float64 CUDA tensor the caller
+    zeroed, which receives the sum of every thread's 64 accumulators."""
+    import torch
+    if ab.dtype != torch.float32 or ab.numel() != 16 or not ab.is_cuda or not ab.is_contiguous():
+        raise ValueError("ffma2: ab must be 16 contiguous float32 on the GPU")
+    if out.dtype != torch.float64 or not out.is_cuda:
+        raise ValueError("ffma2: out must be a float64 CUDA tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    rc = load().tgemm_probe_ffma2(int(warps_per_sm), int(iters), ab.data_ptr(), out.data_ptr(),
+                                  int(stream.cuda_stream))
+    if rc != 0:
+        raise RuntimeError(f"tgemm_probe_ffma2: status {rc}")

@@ -38,13 +38,22 @@ def test_probes_library_exports_its_header_and_checks_arguments():
     names = declared_functions(PROBES_HEADER)
     assert names == sorted(probes.SIGNATURES)
     fake_buf, fake_sum = 0x10000000, 0x20000000
-    for name in names:
+    for name in [n for n in names if n.startswith("tgemm_probe_read_")]:
         fn = getattr(lib, name)
         assert fn(fake_buf, 17, fake_sum, None) == 1          # not a multiple of 16 bytes
         assert fn(fake_buf + 8, 32, fake_sum, None) == 1      # buffer not 16-byte aligned
         assert fn(fake_buf, 32, None, None) == 1              # no sum
         assert fn(fake_buf, -16, fake_sum, None) == 1
         assert fn(None, 0, fake_sum, None) == 0               # empty: nothing queued
+    # the paired-FMA probe's argument rules (refused before any CUDA call)
+    ffma2 = lib.tgemm_probe_ffma2
+    assert ffma2(0, 16, fake_buf, fake_sum, None) == 1        # no warps
+    assert ffma2(17, 16, fake_buf, fake_sum, None) == 1       # more than 16 warps per SM
+    assert ffma2(8, -1, fake_buf, fake_sum, None) == 1
+    assert ffma2(8, 1 << 40, fake_buf, fake_sum, None) == 1
+    assert ffma2(8, 16, None, fake_sum, None) == 1            # no operands
+    assert ffma2(8, 16, fake_buf + 2, fake_sum, None) == 1    # operands not 4-byte aligned
+    assert ffma2(8, 16, fake_buf, fake_sum + 4, None) == 1    # out not 8-byte aligned
 
 
 def test_pages_library_exports_its_header():

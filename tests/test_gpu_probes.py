@@ -1,9 +1,11 @@
-"""The read-stream calibration kernels (include/tgemm_probes.h) on the GPU.
+"""The calibration kernels (include/tgemm_probes.h) on the GPU.
 
-Each probe must read every byte of the buffer exactly once: its checksum (the
-32-bit words added as unsigned integers, modulo 2^64) must equal the one
-computed on the host, for buffer sizes that are and are not multiples of the
-TMA probe's 32 KiB chunk and of the thread counts.
+Each read-stream probe must read every byte of the buffer exactly once: its
+checksum (the 32-bit words added as unsigned integers, modulo 2^64) must
+equal the one computed on the host, for buffer sizes that are and are not
+multiples of the TMA probe's 32 KiB chunk and of the thread counts.  The
+paired-FMA probe must do every one of its FMAs: with power-of-two operands
+its total is exact and known in closed form.
 """
 import numpy as np
 import pytest
@@ -34,3 +36,16 @@ def test_probe_checksum_covers_every_word(how, nbytes):
     want = int(host.astype(np.uint64).sum(dtype=np.uint64))
     got = int(total.cpu().numpy().view(np.uint64)[0])
     assert got == want, (how, nbytes, got, want)
+
+
+@pytest.mark.parametrize("warps", [1, 8, 16])
+@pytest.mark.parametrize("iters", [0, 1, 7, 4096])
+def test_ffma2_probe_does_every_fma(warps, iters):
+    a = [2.0 ** -(i % 4) for i in range(8)]          # 1, 1/2, 1/4, 1/8, ...
+    b = [2.0 ** (j % 3 - 1) for j in range(8)]       # 1/2, 1, 2, ...
+    ab = torch.tensor(a + b, dtype=torch.float32, device="cuda")
+    out = torch.zeros(1, dtype=torch.float64, device="cuda")
+    probes.ffma2(warps, iters, ab, out)
+    torch.cuda.synchronize()
+    threads = torch.cuda.get_device_properties(0).multi_processor_count * 32 * warps
+    assert out.item() == threads * iters * sum(a) * sum(b)
