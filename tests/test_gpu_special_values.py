@@ -71,3 +71,43 @@ def test_nan_and_inf_propagate_like_the_oracle(shape, modes):
         fin = np.isfinite(P)
         assert np.isnan(P).any() and np.isinf(P).any(), what   # the planted values reached the output
         assert np.array_equal(C[fin], P[fin].astype(np.float32)), what
+
+
+def _bf16_bits(x):
+    return (np.asarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+SUBNORMAL = [
+    # label, a, b: every entry of A is a, of B is b, so every C entry is k a b;
+    # a and b are exact in fp32, TF32 and bf16
+    ("subnormal inputs", 2.0 ** -130, 1.0),          # a below 2^-126, result normal
+    ("subnormal products", 2.0 ** -100, 2.0 ** -30),  # each product 2^-130, result normal
+    ("subnormal results", 2.0 ** -130, 2.0 ** -15),   # result k 2^-145, below 2^-126
+]
+
+
+@pytest.mark.parametrize("shape", [(64, 64, 64), (16, 256, 64), (300, 520, 200)], ids=lambda s: "x".join(map(str, s)))
+def test_subnormals(shape):
+    """Subnormal operands, products and results are exact on every path (no
+    flush to zero), as long as the operand itself is representable in the
+    path's input format.  TF32 keeps the top 10 fraction bits of the fp32
+    pattern, so an fp32 subnormal below 2^-136 (here 2^-140) reaches the
+    tensor core as zero, while the FFMA path keeps it."""
+    m, n, k = shape
+    for label, a, b in SUBNORMAL:
+        want = np.float32(np.float64(a) * np.float64(b) * k)
+        for mode in ("f32", "tf32", "bf16"):
+            A = np.full((m, k), a, np.float32)
+            B = np.full((k, n), b, np.float32)
+            if mode == "bf16":
+                A, B = _bf16_bits(A), _bf16_bits(B)
+            C = parity.run(mode, A, B).cpu().numpy()
+            P, _ = oracle.gemm(A, B)
+            assert np.array_equal(P.astype(np.float32), np.full((m, n), want)), (label, mode)   # the oracle, exact
+            assert np.array_equal(C, np.full((m, n), want)), (label, mode, shape, float(C.min()), float(C.max()))
+    # below TF32's window: FFMA exact, TF32 zero
+    A = np.full((m, k), 2.0 ** -140, np.float32)
+    B = np.ones((k, n), np.float32)
+    want = np.float32(k * 2.0 ** -140)
+    assert np.array_equal(parity.run("f32", A, B).cpu().numpy(), np.full((m, n), want))
+    assert np.array_equal(parity.run("tf32", A, B).cpu().numpy(), np.zeros((m, n), np.float32))
