@@ -37,6 +37,7 @@
 // in a fixed order, and a split tile is (head partial) + (tail partial), so
 // repeated runs are bit-identical.
 #include <cstdio>
+#include <cstring>
 
 #include "device.cuh"
 #include "host.h"
@@ -68,10 +69,14 @@ struct Cfg {
     static constexpr int GROUP_M = kWide ? 8 : 16;
     static constexpr uint32_t IDESC =
         instr_desc(kTF32 ? kFormatTF32 : kFormatBF16, 0, kBKMajor ? 0u : 1u, 128, BN);
-    // per epilogue warp a 32 x 32 fp32 tile, rows padded to 36 floats, that turns
-    // TMEM rows into coalesced row segments of C
+    // per epilogue warp two 32 x 32 fp32 staging tiles (4 KiB each) in the
+    // layout of a TMA box with 128-byte swizzle, from which TMA stores write C;
+    // where C's rows are not 16-byte aligned, one tile with rows padded to 36
+    // floats, read back by the warp for scalar stores
     static constexpr int EPI_PITCH = 36;
-    static constexpr uint32_t EPI_BYTES = 4 * 32 * EPI_PITCH * 4;
+    static constexpr uint32_t EPI_BUF = 32 * 32 * 4;
+    static constexpr uint32_t EPI_BYTES = 4 * 2 * EPI_BUF;
+    static_assert(32 * EPI_PITCH * 4 <= 2 * EPI_BUF, "the padded tile fits a warp's staging area");
     static constexpr size_t SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + EPI_BYTES + (2 * STAGES + 4) * 8 + 16;
     static_assert(ACCS * HALVES * 256 <= 512, "accumulators exceed tensor memory");
     static_assert(BN % 32 == 0 && BN <= 256, "tile width");
@@ -105,14 +110,15 @@ __device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;
 template <bool kTF32, bool kBKMajor, bool kWide, int kBN, bool kSK>
 __global__ void __launch_bounds__(kThreads, 1)
 umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-            float* __restrict__ C, int64_t ldc, int M, int N, int K, int vec_store, uint32_t* status,
+            const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int64_t ldc, int M, int N, int K,
+            int vec_store, uint32_t* status,
             float* __restrict__ ws, unsigned* __restrict__ flags) {
     using G = Cfg<kTF32, kBKMajor, kWide, kBN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align_1024(smem_raw);
     uint8_t* sA = smem;
     uint8_t* sB = smem + G::STAGES * G::A_BYTES;
-    float* sEpi = reinterpret_cast<float*>(sB + G::STAGES * G::B_BYTES);   // 4 x 32 x 36 fp32
+    float* sEpi = reinterpret_cast<float*>(sB + G::STAGES * G::B_BYTES);   // 4 warps x 2 x 32 x 32 fp32
     uint64_t* full = reinterpret_cast<uint64_t*>(sB + G::STAGES * G::B_BYTES + G::EPI_BYTES);
     uint64_t* empty = full + G::STAGES;
     uint64_t* acc_full = empty + G::STAGES;    // [2]
@@ -289,7 +295,8 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // waiting at a named barrier.
         const int quarter = warp & 3;   // tensor-memory lanes 32*quarter .. +31
         const int row_in_half = quarter * 32 + lane;
-        float* epi = sEpi + (warp - 2) * 32 * G::EPI_PITCH;   // this warp's 32 x 32 staging tile
+        float* epi = sEpi + (warp - 2) * (2 * G::EPI_BUF / 4);   // this warp's staging area
+        uint32_t stores = 0;   // TMA stores this warp has issued (its staging tiles alternate)
         bool ok = true;
         int it = 0;
         Seq sq;
@@ -353,43 +360,55 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     }
                     // Corner turn (note.jhbae.stream "Lec 29 · GPU Architecture (2)",
                     // transpose case study): lane l holds row l of this 32 x 32 block;
-                    // through the warp's shared tile the warp then writes whole row
-                    // segments, 128 contiguous bytes per row, instead of 32 rows at once.
-                    // Tile rows are 36 floats apart, so the 8 lanes of a quarter warp
-                    // storing 16-byte chunk q of 8 consecutive rows hit 8 different
-                    // bank groups, and a row read back is 128 contiguous bytes.  (An
-                    // XOR-swizzled 32-float row is conflict-free as well, but measured
-                    // slower where C's rows are not 16-byte aligned.)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q)
-                        *reinterpret_cast<float4*>(epi + lane * G::EPI_PITCH + 4 * q) =
-                            make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                        __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-                    __syncwarp();
+                    // through the warp's shared tile C is written as whole 128-byte row
+                    // segments instead of 32 rows at once.
                     const int col0 = tn * G::BN + c * 32;
                     const int row0 = tm * G::BM + h * 128 + quarter * 32;
-                    if (vec_store) {
-                        // 4 rows x 128 bytes per warp store
-                        const int q = lane & 7;
-                        const int col = col0 + 4 * q;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const int rr = 4 * i + (lane >> 3);
-                            const float4 v = *reinterpret_cast<const float4*>(epi + rr * G::EPI_PITCH + 4 * q);
-                            if (row0 + rr < M) {
-                                float* dst = C + static_cast<int64_t>(row0 + rr) * ldc + col;
-                                if (col + 4 <= N) {
-                                    *reinterpret_cast<float4*>(dst) = v;
-                                } else {
-                                    const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                                    for (int j = 0; j < 4; ++j)
-                                        if (col + j < N) dst[j] = e[j];
-                                }
-                            }
+                    // A TMA store clips a row at 16-byte granularity: a block that runs
+                    // past C's last column takes it only if that column ends a 16-byte
+                    // granule (N a multiple of 4).
+                    if (vec_store && (col0 + 32 <= N || (N & 3) == 0)) {
+                        // The tile is a TMA box (32 rows of 128 bytes, 128-byte swizzle:
+                        // 16-byte chunk q of row i at chunk q ^ (i % 8), so the eight rows a
+                        // quarter warp writes fall in eight bank groups); one lane has the
+                        // TMA unit store it, and rows and columns past C are not written.
+                        // The warp moves on while the store drains, into its other tile
+                        // once the store issued two blocks ago has read it.
+                        float* tile_buf = epi + (stores & 1u) * (G::EPI_BUF / 4);
+                        if (stores >= 2) {
+                            if (lane == 0) bulk_wait_group_read<1>();
+                            __syncwarp();
                         }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<float4*>(tile_buf + lane * 32 + ((q ^ (lane & 7)) << 2)) =
+                                make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                            __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                        fence_proxy_async_smem();   // the generic-proxy writes, before the TMA unit reads them
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&tmC, tile_buf, col0, row0);
+                            bulk_commit_group();
+                        }
+                        ++stores;
                     } else {
-                        // one row x 128 bytes per warp store (C rows not 16-byte aligned)
+                        // C rows not 16-byte aligned (TMA cannot describe C), or a block at
+                        // a ragged right edge: rows padded to 36 floats, so the 8 lanes of a
+                        // quarter warp storing 16-byte chunk q of 8 consecutive rows hit 8
+                        // different bank groups; the warp reads each row back (128
+                        // contiguous bytes) and stores it, one row x 128 bytes per warp
+                        // store.  The staging area is free once this warp's TMA stores
+                        // have read it.
+                        if (stores > 0) {
+                            if (lane == 0) bulk_wait_group_read<0>();
+                            __syncwarp();
+                        }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<float4*>(epi + lane * G::EPI_PITCH + 4 * q) =
+                                make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                            __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                        __syncwarp();
                         const int col = col0 + lane;
                         const int q = lane >> 2, w = lane & 3;
 #pragma unroll 8
@@ -397,8 +416,8 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                             const float v = epi[rr * G::EPI_PITCH + 4 * q + w];
                             if (row0 + rr < M && col < N) C[static_cast<int64_t>(row0 + rr) * ldc + col] = v;
                         }
+                        __syncwarp();   // the tile is rewritten by the next block
                     }
-                    __syncwarp();   // the tile is rewritten by the next block
                 }
             }
             tc_fence_before_sync();
@@ -409,6 +428,8 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                 if (threadIdx.x == 64) st_release_u32(flags + blockIdx.x, 1u);
             }
         }
+        // every TMA store of C has completed (and read its staging tile) before the CTA ends
+        if (lane == 0) bulk_wait_group<0>();
     }
 
     __syncthreads();
@@ -468,7 +489,16 @@ cudaError_t launch(const Problem& p, const Device& dev, void* workspace) {
         return err;
     }
     const int64_t tiles = tile_count<kTF32, kBKMajor, kWide, kBN>(p);
-    const int vec_store = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
+    // C through TMA stores (32 x 32 boxes, 128-byte swizzle) where TMA can describe
+    // it: 16-byte aligned base and row pitch; otherwise scalar stores.
+    CUtensorMap tc;
+    std::memset(&tc, 0, sizeof tc);
+    int vec_store = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
+    if (vec_store && !make_tensor_map(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.C, p.m, p.n, p.ldc, 32, 32,
+                                      CU_TENSOR_MAP_SWIZZLE_128B)) {
+        clear_error();
+        vec_store = 0;
+    }
     float* ws = nullptr;
     unsigned* flags = nullptr;
     cudaLaunchConfig_t cfg = {};
@@ -504,7 +534,7 @@ cudaError_t launch(const Problem& p, const Device& dev, void* workspace) {
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    err = cudaLaunchKernelEx(&cfg, kernel, ta, tb, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status, ws, flags);
+    err = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status, ws, flags);
     count_launch();
     if (err != cudaSuccess) set_error("umma_kernel launch: %s", cudaGetErrorString(err));
     return err;

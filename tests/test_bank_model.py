@@ -205,38 +205,51 @@ def test_transpose_strips_cover_the_tile_once():
     assert seen == {(r, c) for r in range(128) for c in range(32)}
 
 
-# ---- tensor-core epilogue (csrc/umma.cu): per-warp 32 x 32 fp32 staging tile ----
-# Lane l holds row l of a 32 x 32 block (one tcgen05.ld); tile rows are padded
-# to 36 floats (144 bytes), 16-byte chunk q of row i at byte 144 i + 16 q.
+# ---- tensor-core epilogue (csrc/umma.cu): per-warp 32 x 32 fp32 staging tiles ----
+# Lane l holds row l of a 32 x 32 block (one tcgen05.ld).  Where TMA can store
+# C, the tile is a TMA box with 128-byte swizzle: 16-byte chunk q of row i at
+# chunk q ^ (i % 8) (byte 128 i + 16 (q ^ (i % 8))).  Otherwise rows are padded
+# to 36 floats (144 bytes) and the warp reads each row back.
 EPI_PITCH = 36
+
+
+def epi_swizzled(row, chunk):
+    return row * 128 + ((chunk ^ (row & 7)) << 4)
 
 
 def epi_offset(row, chunk, word=0):
     return row * 4 * EPI_PITCH + (chunk << 4) + 4 * word
 
 
-def test_epilogue_pitch_matches_the_kernel():
+def test_epilogue_layouts_match_the_kernel():
     src = open(os.path.join(CSRC, "umma.cu")).read()
     assert re.search(r"EPI_PITCH\s*=\s*%d\s*;" % EPI_PITCH, src)
-    assert "4 * 32 * EPI_PITCH * 4" in src
-    assert "epi + lane * G::EPI_PITCH + 4 * q" in src
+    assert "tile_buf + lane * 32 + ((q ^ (lane & 7)) << 2)" in src          # TMA box, 128-byte swizzle
+    assert "CU_TENSOR_MAP_SWIZZLE_128B" in src and "tma_store_2d(&tmC, tile_buf, col0, row0)" in src
+    assert "epi + lane * G::EPI_PITCH + 4 * q" in src                        # padded rows
+
+
+def test_swizzled_tile_is_the_tma_128_byte_swizzle():
+    # the TMA swizzle XORs bits [4, 6] of the byte offset with bits [7, 9]
+    for row in range(32):
+        for q in range(8):
+            logical = row * 128 + q * 16
+            assert epi_swizzled(row, q) == logical ^ (((logical >> 7) & 7) << 4)
+
+
+def test_swizzled_tile_writes_one_pass_per_quarter_warp():
+    for q in range(8):
+        for quarter in range(4):
+            addrs = [epi_swizzled(l, q) for l in range(8 * quarter, 8 * quarter + 8)]
+            assert wavefronts(addrs, width=16) == 1, (q, quarter)
 
 
 def test_epilogue_tile_writes_one_pass_per_quarter_warp():
-    # float4 store of chunk q by every lane: lane l writes row l
+    # padded rows: float4 store of chunk q by every lane, lane l writes row l
     for q in range(8):
         for quarter in range(4):
             addrs = [epi_offset(l, q) for l in range(8 * quarter, 8 * quarter + 8)]
             assert wavefronts(addrs, width=16) == 1, (q, quarter)
-
-
-def test_epilogue_tile_vector_reads_one_pass_per_quarter_warp():
-    # float4 read i: lane reads row 4 i + lane / 8, chunk lane % 8
-    for i in range(8):
-        for quarter in range(4):
-            lanes = range(8 * quarter, 8 * quarter + 8)
-            addrs = [epi_offset(4 * i + (l >> 3), l & 7) for l in lanes]
-            assert wavefronts(addrs, width=16) == 1, (i, quarter)
 
 
 def test_epilogue_tile_scalar_reads_one_pass():
@@ -246,16 +259,9 @@ def test_epilogue_tile_scalar_reads_one_pass():
         assert wavefronts(addrs) == 1, rr
 
 
-def test_epilogue_tile_would_conflict_without_the_padding():
+def test_epilogue_tile_would_conflict_without_swizzle_or_padding():
     plain = lambda row, chunk: row * 128 + (chunk << 4)
     # the row-wise writes of one chunk by 8 rows land in one bank group: 8 passes
     assert wavefronts([plain(l, 3) for l in range(8)], width=16) == 8
 
 
-def test_epilogue_tile_reads_cover_the_block_once():
-    seen = set()
-    for i in range(8):
-        for l in range(32):
-            rr, q = 4 * i + (l >> 3), l & 7
-            seen.add((rr, q))
-    assert seen == {(r, q) for r in range(32) for q in range(8)}

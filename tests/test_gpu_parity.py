@@ -313,3 +313,25 @@ def test_random_views_exact_and_nothing_written_outside_c(mode, case_spec):
     for i in range(m):
         inside[oc + i * (n + pc): oc + i * (n + pc) + n] = True
     assert np.all(np.isnan(host[~inside])), "wrote outside C"
+
+
+# C with 16-byte aligned rows (the tensor-core paths store it with TMA) and a
+# right edge in every position within a 16-byte granule: nothing may be
+# written past column n - 1 (a TMA store clips rows at 16-byte granularity,
+# so a ragged edge block must not take it).
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("n", [657, 658, 659, 660, 33, 250])
+def test_ragged_right_edge_with_aligned_rows(mode, n):
+    m, k = 300, 200
+    case = inputs.random_case(4242 + n, m, n, k, kind="int")
+    A_np, B_np = parity.inputs_for(mode, case)
+    ldc = (n + 3) // 4 * 4 + 4                      # 16-byte pitch, at least 4 guard columns
+    C_buf = torch.full(((m + 1) * ldc,), float("nan"), device="cuda")
+    C = C_buf[: m * ldc].view(m, ldc)[:, :n]
+    parity.ENTRY[mode](parity.to_device(A_np), parity.to_device(B_np), C)
+    torch.cuda.synchronize()
+    P, D = oracle.gemm(A_np, B_np)
+    parity.check(mode, C.cpu().numpy(), P, D, True, f"{mode} ragged edge n={n}")
+    host = C_buf.view(m + 1, ldc).cpu().numpy()
+    assert np.all(np.isnan(host[:m, n:])), f"{mode}: wrote past column {n - 1}"
+    assert np.all(np.isnan(host[m:])), f"{mode}: wrote past row {m - 1}"
