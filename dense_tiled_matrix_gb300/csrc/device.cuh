@@ -149,6 +149,19 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
+// The same copy delivered to every CTA of the cluster whose bit is set in
+// `mask`: the box lands at the same shared-memory offset in each of them and
+// completes transaction bytes on the barrier at `bar`'s offset in each.
+__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                                      int32_t c0, int32_t c1, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%3, %4}], [%2], %5;"
+        :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)),
+           "r"(c0), "r"(c1), "h"(mask)
+        : "memory");
+}
+
 // 2-D tiled bulk copy shared -> global of the box at (c0, c1), added to the
 // thread's current bulk group.  Rows and columns outside the tensor are not
 // written.  c0 and c1 must not be negative.
@@ -236,6 +249,13 @@ __device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  :: "r"(smem_addr(bar)) : "memory");
+}
+
+// As umma_commit, arriving on the barrier at `bar`'s offset in every CTA of
+// the cluster whose bit is set in `mask`.
+__device__ __forceinline__ void umma_commit_multicast(uint64_t* bar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 :: "r"(smem_addr(bar)), "h"(mask) : "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's tensor-memory lane.

@@ -26,12 +26,16 @@
 //  * One thread of warp 1 issues the MMAs: 128 x 256 x (32 bytes of K) per
 //    instruction, accumulating in fp32 in tensor memory.  With 128 x 256
 //    tiles, two accumulators of 256 columns let the epilogue of one tile
-//    overlap the MMAs of the next.
+//    overlap the MMAs of the next.  For large bf16 grids of such tiles, the
+//    two CTAs of a (2 x 1) cluster take vertically adjacent tiles and share
+//    their B tile: each loads half of its chunks with TMA multicast into both.
 //  * Warps 2-5 drain an accumulator with tcgen05.ld (warp w reads lanes
-//    32*(w%4) .. +31, i.e. 32 rows of C, one row per lane), turn each 32 x 32
-//    block through a padded shared tile so that a warp store covers whole
-//    128-byte row segments of C (128-bit stores where C's rows are 16-byte
-//    aligned), masked at the edges of C.
+//    32*(w%4) .. +31, i.e. 32 rows of C, one row per lane) and turn each
+//    32 x 32 block through shared memory so that C is written as whole
+//    128-byte row segments: where TMA can describe C, the block is staged in
+//    the layout of a TMA box and one lane stores it with a TMA store (two
+//    staging tiles per warp alternate); otherwise the warp reads back a
+//    padded tile and stores scalars, masked at the edges of C.
 //
 // Every C element is written exactly once.  The tensor cores add the k terms
 // in a fixed order, and a split tile is (head partial) + (tail partial), so
@@ -85,6 +89,7 @@ struct Cfg {
 
 constexpr int kThreads = 192;
 constexpr bool kPdl = true;   // whole-tile launches may start behind the previous kernel
+constexpr bool kUsePairs = true;   // bf16 128-row whole tiles as multicast CTA pairs
 
 __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, int group_m, int& tm,
                                             int& tn) {
@@ -107,13 +112,18 @@ __device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;
 // its flag; the head waits for the flag, adds that partial to its own
 // accumulator (always head + tail) and stores the tile.  Split tiles need
 // every CTA resident: the launch is cooperative.
-template <bool kTF32, bool kBKMajor, bool kWide, int kBN, bool kSK>
+template <bool kTF32, bool kBKMajor, bool kWide, int kBN, bool kSK, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
 umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int64_t ldc, int M, int N, int K,
             int vec_store, uint32_t* status,
             float* __restrict__ ws, unsigned* __restrict__ flags) {
     using G = Cfg<kTF32, kBKMajor, kWide, kBN>;
+    // kPair: the two CTAs of a (2 x 1) cluster take vertically adjacent 128 x 256
+    // tiles, which use the same B tile: each loads half of its 128-byte chunks and
+    // multicasts them to both, so each SM fetches the operand bytes per MMA of a
+    // 256-row tile while keeping two accumulators.
+    static_assert(!kPair || (!kWide && !kSK && !kBKMajor && G::NCH % 2 == 0), "pairs: bf16 128-row whole tiles");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_align_1024(smem_raw);
     uint8_t* sA = smem;
@@ -136,6 +146,21 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     const int tiles_n = (N + G::BN - 1) / G::BN;
     const int KT = (K + G::BK - 1) / G::BK;
     const int tiles = tiles_m * tiles_n;
+    // Pairs: rank r of cluster c takes tile rows 2 pm + r of the pairs c, c + G / 2, ...
+    const uint32_t rank = kPair ? cluster_cta_rank() : 0u;
+    const int pairs_m = (tiles_m + 1) / 2;
+    const int units = kPair ? pairs_m * tiles_n : tiles;
+    const int unit0 = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+    const int unit_step = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+    auto coords = [&](int unit, int& tm, int& tn) {
+        if (kPair) {
+            int pm;
+            tile_coords(unit, pairs_m, tiles_n, G::GROUP_M / 2, pm, tn);
+            tm = 2 * pm + static_cast<int>(rank);   // past the last tile row: loads read zeros, nothing is stored
+        } else {
+            tile_coords(unit, tiles_m, tiles_n, G::GROUP_M, tm, tn);
+        }
+    };
     SkPlan plan;
     if (kSK) plan.init(tiles, KT, blockIdx.x, gridDim.x);
     // The CTA's segments (tile, k-phases [ka, kz)): with kSK the plan's
@@ -145,14 +170,14 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         int t_next;
     };
     auto seq_init = [&](Seq& q) {
-        q.t_next = blockIdx.x;
+        q.t_next = unit0;
         if (kSK) q.cur.init(plan);
     };
     auto seq_next = [&](Seq& q, int& t, int& ka, int& kz) -> bool {
         if (kSK) return q.cur.next(plan, KT, t, ka, kz);
-        if (q.t_next >= tiles) return false;
+        if (q.t_next >= units) return false;
         t = q.t_next;
-        q.t_next += gridDim.x;
+        q.t_next += unit_step;
         ka = 0;
         kz = KT;
         return true;
@@ -163,7 +188,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         tma_prefetch_map(&tmB);
         for (int s = 0; s < G::STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], kPair ? 2 : 1);   // pairs: both CTAs' MMAs release a stage
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
@@ -178,6 +203,8 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // pairs: the peer's barriers exist before any copy can land in its shared memory
+    if (kPair) cluster_sync_all();
     const uint32_t tmem_base = *tmem_slot;
     // Launched right behind the previous kernel in the stream (e.g. the B
     // transpose of the TF32 path): wait for it before any global access.
@@ -195,7 +222,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             int tile, ka, kz;
             while (ok && seq_next(sq, tile, ka, kz)) {
                 int tm, tn;
-                tile_coords(tile, tiles_m, tiles_n, G::GROUP_M, tm, tn);
+                coords(tile, tm, tn);
                 for (int kb = ka; kb < kz; ++kb) {
                     if (!mbar_wait(&empty[s], ph ^ 1u, status)) { ok = false; break; }
 #ifdef TGEMM_DEBUG
@@ -206,6 +233,14 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     uint8_t* b_dst = sB + s * G::B_BYTES;
                     if (kBKMajor) {
                         tma_load_2d(b_dst, &tmB, &full[s], kb * G::BK, tn * G::BN);
+                    } else if (kPair) {
+                        // this CTA's half of the chunks, into both CTAs of the pair
+#pragma unroll
+                        for (int c = 0; c < G::NCH / 2; ++c) {
+                            const int ch = static_cast<int>(rank) * (G::NCH / 2) + c;
+                            tma_load_2d_multicast(b_dst + ch * G::CH_BYTES, &tmB, &full[s], tn * G::BN + ch * G::CH,
+                                                  kb * G::BK, 0x3);
+                        }
                     } else {
 #pragma unroll
                         for (int c = 0; c < G::NCH; ++c)
@@ -276,7 +311,12 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                 umma_f16(d_tmem + h * G::TCOL, ad, bd, G::IDESC, accumulate);
                         }
                     }
-                    umma_commit(&empty[s]);   // stage free once these MMAs complete
+                    // stage free once these MMAs complete (pairs: in both CTAs, whose
+                    // copies land in each other's stage)
+                    if (kPair)
+                        umma_commit_multicast(&empty[s], 0x3);
+                    else
+                        umma_commit(&empty[s]);
                     last_s = s;
                     last_ph = ph;
                     if (++s == G::STAGES) { s = 0; ph ^= 1u; }
@@ -309,7 +349,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             tc_fence_after_sync();
             __syncwarp();   // tcgen05.ld below is warp-collective
             int tm, tn;
-            tile_coords(tile, tiles_m, tiles_n, G::GROUP_M, tm, tn);
+            coords(tile, tm, tn);
             const bool tail = kSK && ka > 0;
             const bool head = kSK && !tail && kz < KT;
             // Partial tile of a CTA's slot: float4 ((h * BN/32 + c) * 8 + q) * 128 + row
@@ -366,8 +406,10 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                     const int row0 = tm * G::BM + h * 128 + quarter * 32;
                     // A TMA store clips a row at 16-byte granularity: a block that runs
                     // past C's last column takes it only if that column ends a 16-byte
-                    // granule (N a multiple of 4).
-                    if (vec_store && (col0 + 32 <= N || (N & 3) == 0)) {
+                    // granule (N a multiple of 4).  A block wholly below C issues none
+                    // (the scalar path below stores nothing for it).  The conditions
+                    // are uniform across the warp.
+                    if (vec_store && row0 < M && (col0 + 32 <= N || (N & 3) == 0)) {
                         // The tile is a TMA box (32 rows of 128 bytes, 128-byte swizzle:
                         // 16-byte chunk q of row i at chunk q ^ (i % 8), so the eight rows a
                         // quarter warp writes fall in eight bank groups); one lane has the
@@ -433,6 +475,8 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
     }
 
     __syncthreads();
+    // pairs: the peer has consumed every stage, so no copy is still landing in it
+    if (kPair) cluster_sync_all();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after_sync();
@@ -471,7 +515,7 @@ uint64_t workspace_bytes(const Problem& p, const Device& dev) {
 }
 
 // Stream-K (kSK, with its workspace) or whole tiles.
-template <bool kTF32, bool kBKMajor, bool kWide, int kBN, bool kSK>
+template <bool kTF32, bool kBKMajor, bool kWide, int kBN, bool kSK, bool kPair = false>
 cudaError_t launch(const Problem& p, const Device& dev, void* workspace) {
     using G = Cfg<kTF32, kBKMajor, kWide, kBN>;
     const CUtensorMapDataType dt = kTF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -481,7 +525,7 @@ cudaError_t launch(const Problem& p, const Device& dev, void* workspace) {
                  : make_tensor_map(&tb, dt, G::ES, p.B, p.k, p.n, p.ldb, G::BK, G::CH, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!make_tensor_map(&ta, dt, G::ES, p.A, p.m, p.k, p.lda, G::BM, G::BK, CU_TENSOR_MAP_SWIZZLE_128B) || !b_ok)
         return cudaErrorInvalidValue;
-    auto kernel = umma_kernel<kTF32, kBKMajor, kWide, kBN, kSK>;
+    auto kernel = umma_kernel<kTF32, kBKMajor, kWide, kBN, kSK, kPair>;
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(G::SMEM));
     if (err != cudaSuccess) {
@@ -502,18 +546,29 @@ cudaError_t launch(const Problem& p, const Device& dev, void* workspace) {
     float* ws = nullptr;
     unsigned* flags = nullptr;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = G::SMEM;
     cfg.stream = p.stream;
     cfg.gridDim = dim3(static_cast<unsigned>(tiles < dev.sm_count ? tiles : dev.sm_count), 1, 1);
+    cfg.attrs = attr;
     if (!kSK && kPdl) {
         // The prologue (barriers, tensor memory) overlaps the previous kernel's
         // tail; the kernel waits for it before touching global memory.
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        ++cfg.numAttrs;
+    }
+    if (kPair) {
+        // one (2 x 1) cluster per pair of tile rows, persistent over the pairs
+        const int64_t pairs = static_cast<int64_t>((p.m + 2 * G::BM - 1) / (2 * G::BM)) * ((p.n + G::BN - 1) / G::BN);
+        const int64_t clusters = pairs < dev.sm_count / 2 ? pairs : dev.sm_count / 2;
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = 2;
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
     }
     if (kSK) {
         if (!workspace) {
@@ -531,7 +586,6 @@ cudaError_t launch(const Problem& p, const Device& dev, void* workspace) {
         attr[0].id = cudaLaunchAttributeCooperative;   // all CTAs resident: a head may wait for its tail
         attr[0].val.cooperative = 1;
         cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count), 1, 1);
-        cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
     err = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status, ws, flags);
@@ -544,6 +598,17 @@ template <bool kTF32, bool kBKMajor, bool kWide, int kBN>
 cudaError_t launch_any(const Problem& p, const Device& dev, void* workspace) {
     if (workspace && has_sk<kTF32, kBKMajor, kWide, kBN>(p, dev))
         return launch<kTF32, kBKMajor, kWide, kBN, true>(p, dev, workspace);
+    if constexpr (!kTF32 && !kBKMajor && !kWide) {
+        // Pairs where the tile rows pair up evenly and fill at least two rounds.
+        // Measured on GB300 (us per launch, single CTAs -> pairs): 8192 x 8192 x
+        // 2048 201.4 -> 194.6, 8192 x 8192 x 1024 120.6 -> 116.3, 6144 x 6144 x
+        // 2048 113.8 -> 110.8, 3000 x 6000 x 1024 39.8 -> 39.3; but 4097 x 3001 x
+        // 1023 (33 tile rows: one pair half empty) 50.3 -> 57.2 and 1000 x 1001 x
+        // 999 (32 tiles) 27.3 -> 28.6.
+        const int64_t tiles_m = (p.m + 127) / 128;
+        if (kUsePairs && tiles_m % 2 == 0 && tile_count<kTF32, kBKMajor, kWide, kBN>(p) >= 2 * dev.sm_count)
+            return launch<kTF32, kBKMajor, kWide, kBN, false, true>(p, dev, nullptr);
+    }
     return launch<kTF32, kBKMajor, kWide, kBN, false>(p, dev, nullptr);
 }
 

@@ -335,3 +335,18 @@ def test_ragged_right_edge_with_aligned_rows(mode, n):
     host = C_buf.view(m + 1, ldc).cpu().numpy()
     assert np.all(np.isnan(host[:m, n:])), f"{mode}: wrote past column {n - 1}"
     assert np.all(np.isnan(host[m:])), f"{mode}: wrote past row {m - 1}"
+
+
+# bf16 128-row tiles as multicast CTA pairs (an even number of tile rows and at
+# least two rounds of tiles on GB300): whole output against the oracle, exact
+# sizes, ragged m / n / k (the last tile row partly empty) and short k.
+PAIR_SHAPES = [(2560, 4352, 1024), (2500, 4100, 999), (4096, 2432, 200)]
+
+
+@pytest.mark.parametrize("shape", PAIR_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_bf16_cta_pairs(shape):
+    m, n, k = shape
+    assert ((m + 127) // 128) % 2 == 0 and ((m + 127) // 128) * ((n + 255) // 256) >= 2 * 152
+    parity.full_check("bf16", inputs.random_case(8100 + m + n + k, m, n, k, kind="int"), f"bf16 pairs int {shape}")
+    parity.full_check("bf16", inputs.random_case(8200 + m + n + k, m, n, k, kind="normal"),
+                      f"bf16 pairs normal {shape}")
