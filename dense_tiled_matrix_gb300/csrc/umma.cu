@@ -29,13 +29,13 @@
 //    overlap the MMAs of the next.  For large bf16 grids of such tiles, the
 //    two CTAs of a (2 x 1) cluster take vertically adjacent tiles and share
 //    their B tile: each loads half of its chunks with TMA multicast into both.
-//  * Warps 2-5 drain an accumulator with tcgen05.ld (warp w reads lanes
-//    32*(w%4) .. +31, i.e. 32 rows of C, one row per lane) and turn each
-//    32 x 32 block through shared memory so that C is written as whole
-//    128-byte row segments: where TMA can describe C, the block is staged in
-//    the layout of a TMA box and one lane stores it with a TMA store (two
-//    staging tiles per warp alternate); otherwise the warp reads back a
-//    padded tile and stores scalars, masked at the edges of C.
+//  * Warps 2-9 drain an accumulator with tcgen05.ld (warp w reads lanes
+//    32*(w%4) .. +31, i.e. 32 rows of C, one row per lane; the two warps of a
+//    lane quarter take alternate 32-column blocks) and turn each 32 x 32
+//    block through shared memory so that C is written as whole 128-byte row
+//    segments: the block is staged in the layout of a TMA box and, where TMA
+//    can describe C, one lane stores it with a TMA store; otherwise the warp
+//    reads the rows back and stores scalars, masked at the edges of C.
 //
 // Every C element is written exactly once.  The tensor cores add the k terms
 // in a fixed order, and a split tile is (head partial) + (tail partial), so
@@ -49,6 +49,10 @@
 
 namespace tgemm {
 namespace {
+
+// Epilogue warps: 4 (one per tensor-memory lane quarter, two staging tiles
+// each) or 8 (two per quarter taking alternate column blocks, one tile each).
+constexpr int kMaxEpiWarps = 8;
 
 template <bool kTF32, bool kBKMajor, bool kWide, int kBN = 256>
 struct Cfg {
@@ -73,21 +77,18 @@ struct Cfg {
     static constexpr int GROUP_M = kWide ? 8 : 16;
     static constexpr uint32_t IDESC =
         instr_desc(kTF32 ? kFormatTF32 : kFormatBF16, 0, kBKMajor ? 0u : 1u, 128, BN);
-    // per epilogue warp two 32 x 32 fp32 staging tiles (4 KiB each) in the
-    // layout of a TMA box with 128-byte swizzle, from which TMA stores write C;
-    // where C's rows are not 16-byte aligned, one tile with rows padded to 36
-    // floats, read back by the warp for scalar stores
-    static constexpr int EPI_PITCH = 36;
+    // per epilogue warp one 32 x 32 fp32 staging tile (4 KiB) in the layout of
+    // a TMA box with 128-byte swizzle, from which a TMA store writes C (or which
+    // the warp reads back where TMA cannot describe C)
     static constexpr uint32_t EPI_BUF = 32 * 32 * 4;
-    static constexpr uint32_t EPI_BYTES = 4 * 2 * EPI_BUF;
-    static_assert(32 * EPI_PITCH * 4 <= 2 * EPI_BUF, "the padded tile fits a warp's staging area");
+    static constexpr uint32_t EPI_BYTES = kMaxEpiWarps * EPI_BUF;   // 4 warps x 2 tiles or 8 x 1
     static constexpr size_t SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + EPI_BYTES + (2 * STAGES + 4) * 8 + 16;
     static_assert(ACCS * HALVES * 256 <= 512, "accumulators exceed tensor memory");
     static_assert(BN % 32 == 0 && BN <= 256, "tile width");
     static_assert(kBKMajor || BN % CH == 0, "an N-contiguous B tile is a whole number of 128-byte chunks");
 };
 
-constexpr int kThreads = 192;
+constexpr int threads_for(int epi_warps) { return 32 * (2 + epi_warps); }   // producer, MMA issuer, epilogue
 constexpr bool kPdl = true;   // whole-tile launches may start behind the previous kernel
 constexpr bool kUsePairs = true;   // bf16 128-row whole tiles as multicast CTA pairs
 
@@ -103,7 +104,8 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
 }
 
 // Named barrier of the four epilogue warps (threads 64 .. 191).
-__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+template <int kEpiWarps>
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, %0;" :: "n"(32 * kEpiWarps) : "memory"); }
 
 // The CTAs walk the persistent plan of stream_k.cuh: whole tiles b, b + G, ...
 // and, when `ws` is given and the last wave would be partial, a stream-K
@@ -112,8 +114,8 @@ __device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;
 // its flag; the head waits for the flag, adds that partial to its own
 // accumulator (always head + tail) and stores the tile.  Split tiles need
 // every CTA resident: the launch is cooperative.
-template <bool kTF32, bool kBKMajor, bool kWide, int kBN, bool kSK, bool kPair>
-__global__ void __launch_bounds__(kThreads, 1)
+template <bool kTF32, bool kBKMajor, bool kWide, int kBN, bool kSK, bool kPair, int kEpiWarps>
+__global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
 umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int64_t ldc, int M, int N, int K,
             int vec_store, uint32_t* status,
@@ -192,7 +194,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&acc_full[a], 1);
-            mbar_init(&acc_empty[a], 128);
+            mbar_init(&acc_empty[a], 32 * kEpiWarps);
         }
 #ifdef TGEMM_DEBUG
         for (int s = 0; s < G::STAGES; ++s) dbg_fills[s] = 0;
@@ -335,8 +337,14 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         // waiting at a named barrier.
         const int quarter = warp & 3;   // tensor-memory lanes 32*quarter .. +31
         const int row_in_half = quarter * 32 + lane;
-        float* epi = sEpi + (warp - 2) * (2 * G::EPI_BUF / 4);   // this warp's staging area
-        uint32_t stores = 0;   // TMA stores this warp has issued (its staging tiles alternate)
+        static_assert(kEpiWarps == 4 || kEpiWarps == 8, "epilogue warps");
+        // this warp's staging area: two tiles (4 warps) or one (8 warps)
+        float* epi = sEpi + (warp - 2) * (G::EPI_BUF / 4) * (kMaxEpiWarps / kEpiWarps);
+        // With 8 warps two share each lane quarter; member `col_half` drains the
+        // 32-column blocks c = col_half, col_half + 2, ...
+        constexpr int kColStep = kEpiWarps / 4;
+        const int col_half = (warp - 2) / 4;
+        uint32_t stores = 0;   // TMA stores this warp has issued
         bool ok = true;
         int it = 0;
         Seq sq;
@@ -365,14 +373,14 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                                         wait_flag(flags + blockIdx.x + 1, status)
                                     ? 1
                                     : 0;
-                epilogue_sync();
+                epilogue_sync<kEpiWarps>();
             }
 #pragma unroll
             for (int h = 0; h < G::HALVES; ++h) {
                 const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        (acc * G::HALVES + h) * G::TCOL;
 #pragma unroll 1
-                for (int c = 0; c < G::BN / 32; ++c) {
+                for (int c = col_half; c < G::BN / 32; c += kColStep) {
                     uint32_t r[32];
                     // columns of this load inside the allocation (uniform across the warp)
                     (void)TGEMM_DCHECK((acc * G::HALVES + h) * G::TCOL + c * 32 + 32 <= G::TMEM_COLS, status,
@@ -414,11 +422,18 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         // 16-byte chunk q of row i at chunk q ^ (i % 8), so the eight rows a
                         // quarter warp writes fall in eight bank groups); one lane has the
                         // TMA unit store it, and rows and columns past C are not written.
-                        // The warp moves on while the store drains, into its other tile
-                        // once the store issued two blocks ago has read it.
-                        float* tile_buf = epi + (stores & 1u) * (G::EPI_BUF / 4);
-                        if (stores >= 2) {
-                            if (lane == 0) bulk_wait_group_read<1>();
+                        // The warp moves on while the store drains, into its other tile (4
+                        // warps) once the store issued two blocks ago has read it, or into
+                        // the same tile (8 warps) once the last store has.
+                        float* tile_buf = epi;
+                        if (kEpiWarps == 4) {
+                            tile_buf = epi + (stores & 1u) * (G::EPI_BUF / 4);
+                            if (stores >= 2) {
+                                if (lane == 0) bulk_wait_group_read<1>();
+                                __syncwarp();
+                            }
+                        } else if (stores >= 1) {
+                            if (lane == 0) bulk_wait_group_read<0>();
                             __syncwarp();
                         }
 #pragma unroll
@@ -435,19 +450,18 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         ++stores;
                     } else {
                         // C rows not 16-byte aligned (TMA cannot describe C), or a block at
-                        // a ragged right edge: rows padded to 36 floats, so the 8 lanes of a
-                        // quarter warp storing 16-byte chunk q of 8 consecutive rows hit 8
-                        // different bank groups; the warp reads each row back (128
-                        // contiguous bytes) and stores it, one row x 128 bytes per warp
-                        // store.  The staging area is free once this warp's TMA stores
-                        // have read it.
+                        // a ragged right edge: the warp writes the same swizzled tile, reads
+                        // each row back (its 8 chunks are 128 contiguous bytes of one row,
+                        // so the reads are conflict-free too) and stores it, one row x 128
+                        // bytes per warp store.  The tile is free once this warp's TMA
+                        // stores have read it.
                         if (stores > 0) {
                             if (lane == 0) bulk_wait_group_read<0>();
                             __syncwarp();
                         }
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
-                            *reinterpret_cast<float4*>(epi + lane * G::EPI_PITCH + 4 * q) =
+                            *reinterpret_cast<float4*>(epi + lane * 32 + ((q ^ (lane & 7)) << 2)) =
                                 make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
                                             __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
                         __syncwarp();
@@ -455,7 +469,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
                         const int q = lane >> 2, w = lane & 3;
 #pragma unroll 8
                         for (int rr = 0; rr < 32; ++rr) {
-                            const float v = epi[rr * G::EPI_PITCH + 4 * q + w];
+                            const float v = epi[rr * 32 + ((q ^ (rr & 7)) << 2) + w];
                             if (row0 + rr < M && col < N) C[static_cast<int64_t>(row0 + rr) * ldc + col] = v;
                         }
                         __syncwarp();   // the tile is rewritten by the next block
@@ -466,7 +480,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             mbar_arrive(&acc_empty[acc]);
             if (tail) {
                 __threadfence();
-                epilogue_sync();
+                epilogue_sync<kEpiWarps>();
                 if (threadIdx.x == 64) st_release_u32(flags + blockIdx.x, 1u);
             }
         }
@@ -525,13 +539,6 @@ cudaError_t launch(const Problem& p, const Device& dev, void* workspace) {
                  : make_tensor_map(&tb, dt, G::ES, p.B, p.k, p.n, p.ldb, G::BK, G::CH, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!make_tensor_map(&ta, dt, G::ES, p.A, p.m, p.k, p.lda, G::BM, G::BK, CU_TENSOR_MAP_SWIZZLE_128B) || !b_ok)
         return cudaErrorInvalidValue;
-    auto kernel = umma_kernel<kTF32, kBKMajor, kWide, kBN, kSK, kPair>;
-    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(G::SMEM));
-    if (err != cudaSuccess) {
-        set_error("cudaFuncSetAttribute(umma_kernel): %s", cudaGetErrorString(err));
-        return err;
-    }
     const int64_t tiles = tile_count<kTF32, kBKMajor, kWide, kBN>(p);
     // C through TMA stores (32 x 32 boxes, 128-byte swizzle) where TMA can describe
     // it: 16-byte aligned base and row pitch; otherwise scalar stores.
@@ -543,11 +550,27 @@ cudaError_t launch(const Problem& p, const Device& dev, void* workspace) {
         clear_error();
         vec_store = 0;
     }
+    // Eight epilogue warps where the epilogue weighs most (stream-K hand-overs,
+    // scalar stores), four otherwise.  Measured on GB300 (us per launch, 4 -> 8
+    // warps): bf16 3300 x 3000 x 3100 (stream-K) 80.7 -> 73.0, 2000 x 2600 x 1000
+    // (stream-K) 33.6 -> 29.5, 4097 x 3001 x 1023 (C unaligned) 50.5 -> 40.9,
+    // TF32 3300 x 3000 x 3100 126.5 -> 119.7; but aligned C in whole tiles
+    // 8192 x 8192 x 2048 198.9 -> 201.2, 4096 x 4096 x 1024 39.0 -> 40.8,
+    // 2048^3 20.6 -> 21.2 and 8192^3 unchanged.
+    const bool epi8 = kSK || !vec_store;
+    auto kernel = epi8 ? umma_kernel<kTF32, kBKMajor, kWide, kBN, kSK, kPair, 8>
+                       : umma_kernel<kTF32, kBKMajor, kWide, kBN, kSK, kPair, 4>;
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(G::SMEM));
+    if (err != cudaSuccess) {
+        set_error("cudaFuncSetAttribute(umma_kernel): %s", cudaGetErrorString(err));
+        return err;
+    }
     float* ws = nullptr;
     unsigned* flags = nullptr;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads_for(epi8 ? 8 : 4)), 1, 1);
     cfg.dynamicSmemBytes = G::SMEM;
     cfg.stream = p.stream;
     cfg.gridDim = dim3(static_cast<unsigned>(tiles < dev.sm_count ? tiles : dev.sm_count), 1, 1);

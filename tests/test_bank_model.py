@@ -17,7 +17,7 @@ reads, 4 for the B reads on GB300 -- and bank conflicts would add to it); the
 TMA 64-byte swizzle it relies on is
 checked against the kernel's own chunk formula.  So are the TMA transpose's
 reads of a 128-byte-swizzled input tile and its writes of the output tile, and
-the tensor-core epilogue's padded staging tile.
+the tensor-core epilogue's staging tile.
 """
 import os
 import re
@@ -205,28 +205,23 @@ def test_transpose_strips_cover_the_tile_once():
     assert seen == {(r, c) for r in range(128) for c in range(32)}
 
 
-# ---- tensor-core epilogue (csrc/umma.cu): per-warp 32 x 32 fp32 staging tiles ----
-# Lane l holds row l of a 32 x 32 block (one tcgen05.ld).  Where TMA can store
-# C, the tile is a TMA box with 128-byte swizzle: 16-byte chunk q of row i at
-# chunk q ^ (i % 8) (byte 128 i + 16 (q ^ (i % 8))).  Otherwise rows are padded
-# to 36 floats (144 bytes) and the warp reads each row back.
-EPI_PITCH = 36
+# ---- tensor-core epilogue (csrc/umma.cu): per-warp 32 x 32 fp32 staging tile ----
+# Lane l holds row l of a 32 x 32 block (one tcgen05.ld).  The tile is a TMA
+# box with 128-byte swizzle: 16-byte chunk q of row i at chunk q ^ (i % 8)
+# (byte 128 i + 16 (q ^ (i % 8))).  A TMA store reads it where TMA can
+# describe C; otherwise the warp reads each row back, lane l taking word l.
 
 
-def epi_swizzled(row, chunk):
-    return row * 128 + ((chunk ^ (row & 7)) << 4)
+def epi_swizzled(row, chunk, word=0):
+    return row * 128 + ((chunk ^ (row & 7)) << 4) + 4 * word
 
 
-def epi_offset(row, chunk, word=0):
-    return row * 4 * EPI_PITCH + (chunk << 4) + 4 * word
-
-
-def test_epilogue_layouts_match_the_kernel():
+def test_epilogue_layout_matches_the_kernel():
     src = open(os.path.join(CSRC, "umma.cu")).read()
-    assert re.search(r"EPI_PITCH\s*=\s*%d\s*;" % EPI_PITCH, src)
-    assert "tile_buf + lane * 32 + ((q ^ (lane & 7)) << 2)" in src          # TMA box, 128-byte swizzle
+    assert "tile_buf + lane * 32 + ((q ^ (lane & 7)) << 2)" in src           # TMA path
+    assert "epi + lane * 32 + ((q ^ (lane & 7)) << 2)" in src                # read-back path, same layout
+    assert "epi[rr * 32 + ((q ^ (rr & 7)) << 2) + w]" in src
     assert "CU_TENSOR_MAP_SWIZZLE_128B" in src and "tma_store_2d(&tmC, tile_buf, col0, row0)" in src
-    assert "epi + lane * G::EPI_PITCH + 4 * q" in src                        # padded rows
 
 
 def test_swizzled_tile_is_the_tma_128_byte_swizzle():
@@ -238,28 +233,22 @@ def test_swizzled_tile_is_the_tma_128_byte_swizzle():
 
 
 def test_swizzled_tile_writes_one_pass_per_quarter_warp():
+    # float4 store of chunk q by every lane: lane l writes row l
     for q in range(8):
         for quarter in range(4):
             addrs = [epi_swizzled(l, q) for l in range(8 * quarter, 8 * quarter + 8)]
             assert wavefronts(addrs, width=16) == 1, (q, quarter)
 
 
-def test_epilogue_tile_writes_one_pass_per_quarter_warp():
-    # padded rows: float4 store of chunk q by every lane, lane l writes row l
-    for q in range(8):
-        for quarter in range(4):
-            addrs = [epi_offset(l, q) for l in range(8 * quarter, 8 * quarter + 8)]
-            assert wavefronts(addrs, width=16) == 1, (q, quarter)
-
-
-def test_epilogue_tile_scalar_reads_one_pass():
-    # unaligned C: the warp reads one row, lane l takes word l (chunk l / 4, word l % 4)
+def test_swizzled_tile_row_reads_one_pass():
+    # read-back: the warp reads row rr, lane l takes word l (chunk l / 4, word l % 4)
     for rr in range(32):
-        addrs = [epi_offset(rr, l >> 2, l & 3) for l in range(32)]
+        addrs = [epi_swizzled(rr, l >> 2, l & 3) for l in range(32)]
         assert wavefronts(addrs) == 1, rr
+        assert sorted(addrs) == [rr * 128 + 4 * w for w in range(32)]   # exactly the row's 32 words
 
 
-def test_epilogue_tile_would_conflict_without_swizzle_or_padding():
+def test_epilogue_tile_would_conflict_without_the_swizzle():
     plain = lambda row, chunk: row * 128 + (chunk << 4)
     # the row-wise writes of one chunk by 8 rows land in one bank group: 8 passes
     assert wavefronts([plain(l, 3) for l in range(8)], width=16) == 8

@@ -63,7 +63,8 @@ GB300 = dict(max_threads=2048, max_blocks=32, smem_per_sm=228 * 1024, regs_per_s
 @pytest.mark.parametrize("name,threads,smem,regs,expect", [
     ("ffma_f32_ws_kernel", 384, 132224, 168, 1),      # 168 at launch: 24 (producers) / 240 (consumers)
     ("ffma_f32_reduce_kernel", 256, 0, 112, 2),      # 106 registers allocate as 112
-    ("umma_kernel (wide or narrow)", 192, 230512, 120, 1),   # 72-118 registers; 192 KiB ring + 32 KiB staging
+    ("umma_kernel, 4 epilogue warps", 192, 230512, 128, 1),   # 192 KiB ring + 32 KiB staging
+    ("umma_kernel, 8 epilogue warps", 320, 230512, 128, 1),   # 75-127 registers
     ("umma_skinny_kernel<16>", 128, 74840, 32, 3),
     ("transpose_tma_kernel", 256, 99360, 40, 2),
 ])
