@@ -29,9 +29,10 @@
 //    overlap the MMAs of the next.  For large bf16 grids of such tiles, the
 //    two CTAs of a (2 x 1) cluster take vertically adjacent tiles and share
 //    their B tile: each loads half of its chunks with TMA multicast into both.
-//  * Warps 2-9 drain an accumulator with tcgen05.ld (warp w reads lanes
-//    32*(w%4) .. +31, i.e. 32 rows of C, one row per lane; the two warps of a
-//    lane quarter take alternate 32-column blocks) and turn each 32 x 32
+//  * Warps 2-5, or 2-9 for stream-K and C that TMA cannot describe, drain an
+//    accumulator with tcgen05.ld (warp w reads lanes 32*(w%4) .. +31, i.e. 32
+//    rows of C, one row per lane; with 8 warps the two of a lane quarter take
+//    alternate 32-column blocks) and turn each 32 x 32
 //    block through shared memory so that C is written as whole 128-byte row
 //    segments: the block is staged in the layout of a TMA box and, where TMA
 //    can describe C, one lane stores it with a TMA store; otherwise the warp
