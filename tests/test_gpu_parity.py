@@ -337,16 +337,37 @@ def test_ragged_right_edge_with_aligned_rows(mode, n):
     assert np.all(np.isnan(host[m:])), f"{mode}: wrote past row {m - 1}"
 
 
-# bf16 128-row tiles as multicast CTA pairs (an even number of tile rows and at
-# least two rounds of tiles on GB300): whole output against the oracle, exact
-# sizes, ragged m / n / k (the last tile row partly empty) and short k.
-PAIR_SHAPES = [(2560, 4352, 1024), (2500, 4100, 999), (4096, 2432, 200)]
+# bf16 128-row tiles as multicast CTA pairs (k < 3072, no stream-K region, an
+# even number of tile rows and at least two rounds of tiles on GB300): whole
+# output against the oracle, exact sizes, ragged m / n / k (the last tile row
+# partly empty) and short k.
+PAIR_SHAPES = [(2048, 4864, 1024), (2000, 4800, 999), (4096, 2432, 200)]
+
+
+def takes_pairs(m, n, k, sms=152):
+    """The launcher's choice, restated: 128 x 256 tiles (k < 3072), no stream-K
+    (no region, or whole tiles filling at least 3/4 of their rounds), tile rows
+    in pairs, at least two rounds."""
+    tiles_m, tiles_n, kt = (m + 127) // 128, (n + 255) // 256, (k + 63) // 64
+    tiles = tiles_m * tiles_n
+    r = tiles % sms
+    region = tiles >= sms and r > 0 and r * kt >= sms
+    waves = (tiles + sms - 1) // sms
+    stream_k = region and 4 * tiles < 3 * waves * sms
+    return k < 3072 and not stream_k and tiles_m % 2 == 0 and tiles >= 2 * sms
+
+
+def test_pair_rule_restatement():
+    assert takes_pairs(8192, 8192, 2048) and takes_pairs(6144, 6144, 2048)
+    assert not takes_pairs(4097, 3001, 1023)        # 33 tile rows
+    assert not takes_pairs(2560, 4352, 1024)        # stream-K: 340 tiles fill 75 % of 3 rounds
+    assert not takes_pairs(8192, 8192, 8192)        # 256-row tiles
 
 
 @pytest.mark.parametrize("shape", PAIR_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_bf16_cta_pairs(shape):
     m, n, k = shape
-    assert ((m + 127) // 128) % 2 == 0 and ((m + 127) // 128) * ((n + 255) // 256) >= 2 * 152
+    assert takes_pairs(m, n, k)
     parity.full_check("bf16", inputs.random_case(8100 + m + n + k, m, n, k, kind="int"), f"bf16 pairs int {shape}")
     parity.full_check("bf16", inputs.random_case(8200 + m + n + k, m, n, k, kind="normal"),
                       f"bf16 pairs normal {shape}")
