@@ -371,3 +371,23 @@ def test_bf16_cta_pairs(shape):
     parity.full_check("bf16", inputs.random_case(8100 + m + n + k, m, n, k, kind="int"), f"bf16 pairs int {shape}")
     parity.full_check("bf16", inputs.random_case(8200 + m + n + k, m, n, k, kind="normal"),
                       f"bf16 pairs normal {shape}")
+
+
+def test_bf16_cta_pairs_with_unaligned_c():
+    """Pairs with C that TMA cannot describe (row pitch n + 1): the pair kernel
+    with eight epilogue warps on the read-back path; NaN guard columns must
+    stay untouched."""
+    m, n, k = 2048, 4864, 1024
+    assert takes_pairs(m, n, k)
+    case = inputs.random_case(8300, m, n, k, kind="int")
+    A_np, B_np = parity.inputs_for("bf16", case)
+    ldc = n + 1
+    C_buf = torch.full((m * ldc + 8,), float("nan"), device="cuda")
+    C = C_buf[: m * ldc].view(m, ldc)[:, :n]
+    parity.ENTRY["bf16"](parity.to_device(A_np), parity.to_device(B_np), C)
+    torch.cuda.synchronize()
+    P, D = oracle.gemm(A_np, B_np)
+    parity.check("bf16", C.cpu().numpy(), P, D, True, "bf16 pairs, unaligned C")
+    host = C_buf[: m * ldc].view(m, ldc).cpu().numpy()
+    assert np.all(np.isnan(host[:, n:])), "wrote past column n - 1"
+    assert np.all(np.isnan(C_buf[m * ldc:].cpu().numpy()))
