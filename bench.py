@@ -92,7 +92,7 @@ EXTRAS = {
 }
 SLOW_EXTRAS = {"pages_naive_4096", "pages_tiled16_4096", "pages_tiled32_4096"}
 SLOW_EXTRA_ITERS = 4   # timed launches of the pages' kernels at 4096^3 (tens of ms each)
-KERNEL_NAMES = {"f32": "ffma_f32_ws_kernel (912 tiles, then 448 split pieces) + ffma_f32_reduce_kernel (one tgemm_f32 call)", "tf32": "umma_kernel<1, 1, 1, 224, 0>", "bf16": "umma_kernel<0, 0, 1, 256, 0>"}
+KERNEL_NAMES = {"f32": "ffma_f32_ws_kernel (912 tiles, then 448 split pieces) + ffma_f32_reduce_kernel (one tgemm_f32 call)", "tf32": "transpose_tma_kernel + umma_kernel<1, 1, 1, 224, 0, 0, 4>", "bf16": "umma_kernel<0, 0, 1, 256, 0, 0, 4>"}
 
 
 def source_digest(files):

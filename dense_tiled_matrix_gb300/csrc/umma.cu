@@ -6,8 +6,10 @@
 // page's Pvalue) moved into tensor memory and the per-phase inner product done
 // by tcgen05.mma:
 //
-//  * Output tiles of 256 x BN (k >= 3072: two 128-row MMAs share each B tile,
-//    one accumulator spanning the tensor memory, 3 stages) or 128 x BN (two
+//  * Output tiles of 256 x BN (k >= 3072, or k >= 1024 where their rounds of
+//    CTAs fill at least as well as those of 128-row tiles, without stream-K:
+//    two 128-row MMAs share each B tile, one
+//    accumulator spanning the tensor memory, 3 stages) or 128 x BN (two
 //    accumulators, 4 stages), BN = 256, or 224 for TF32 shapes whose last wave
 //    that fills better; visited by a persistent grid of one CTA per SM in
 //    groups of tile rows (neighbouring CTAs share A and B tiles in L2).  Where
@@ -641,9 +643,36 @@ cudaError_t launch_any(const Problem& p, const Device& dev, void* workspace) {
 // Wide 256 x 256 tiles need two thirds of the operand bytes per MMA cycle of
 // the 128 x 256 ones, which hides the L2 latency of the TMA loads better, but
 // their epilogue cannot overlap the next tile's MMAs.  Measured on GB300
-// (bf16): 8192^3 1726 vs 1641 TFLOP/s, 4096^3 1308 vs 1272, but
-// 8192 x 8192 x 2048 1235 vs 1346: long k favours the wide tiles.
-constexpr int kWideMinK = 3072;
+// (bf16): 8192^3 1726 vs 1641 TFLOP/s, 4096^3 1308 vs 1272.  With the TMA-store
+// epilogue they also win at shorter k where their rounds of CTAs are at least
+// as full as those of the 128-row tiles and need no stream-K (us per launch,
+// 128-row -> wide tiles; bf16 2900 x 5000 x 1030 56.8 -> 51.0, 3000 x 6000 x
+// 1024 42.4 -> 39.1, 2048 x 4864 x 2048 32.7 -> 30.7, 4096 x 4096 x 2048 57.3
+// -> 55.2; TF32 4096 x 4096 x 1024 59.1 -> 56.8, 2900 x 5000 x 1030 79.7 ->
+// 73.6; equal fill and no gain at 4096 x 4096 x 1024 and 6144 x 3072 x 1024
+// bf16).  They lose where their rounds are emptier (1536 x 9728 x 1024: 228
+// wide tiles fill 3/4 of two rounds, 456 narrow ones three rounds exactly;
+// bf16 30.6 -> 36.7), where they are too few (2048^3: 64 wide tiles) and
+// where they would be split along k.
+constexpr int kWideMinK = 3072;   // wide tiles from here on
+constexpr int kWideMidK = 1024;   // from here, wide where the rounds fill at least as well
+
+bool use_wide(const Problem& p, const Device& dev, bool tf32) {
+    if (p.k >= kWideMinK) return true;
+    if (p.k < kWideMidK) return false;
+    const bool sk_wide = tf32 ? has_sk<true, true, true, 256>(p, dev) : has_sk<false, false, true, 256>(p, dev);
+    if (sk_wide) return false;
+    const int64_t G = dev.sm_count;
+    // filled fraction of the occupied CTA slots (stream-K fills them all)
+    auto fill = [&](int64_t tiles, int64_t bm) {
+        return static_cast<double>(p.m) * p.n / (static_cast<double>((tiles + G - 1) / G * G) * bm * 256);
+    };
+    const double wide = fill(tf32 ? tile_count<true, true, true, 256>(p) : tile_count<false, false, true, 256>(p), 256);
+    const bool sk_narrow = tf32 ? has_sk<true, true, false, 256>(p, dev) : has_sk<false, false, false, 256>(p, dev);
+    const double narrow =
+        sk_narrow ? 1.0 : fill(tf32 ? tile_count<true, true, false, 256>(p) : tile_count<false, false, false, 256>(p), 128);
+    return wide >= narrow;
+}
 
 // Tile width of the TF32 kernels: 224 instead of 256 when 256-wide tiles
 // would not take stream-K and 224-wide ones fill the occupied CTA slots
@@ -654,7 +683,7 @@ constexpr int kWideMinK = 3072;
 // 96 % filled, against 84 %); 2048 x 2048 x 8192 377 -> 392.  With
 // stream-K the wider tile is better (3300 x 3000 x 3100: 479 against 411).
 bool tf32_narrow_n(const Problem& p, const Device& dev) {
-    const bool wide = p.k >= kWideMinK;
+    const bool wide = use_wide(p, dev, true);
     if (wide ? has_sk<true, true, true, 256>(p, dev) : has_sk<true, true, false, 256>(p, dev)) return false;
     const int64_t bm = wide ? 256 : 128, G = dev.sm_count;
     auto fill = [&](int64_t bn) {
@@ -666,7 +695,7 @@ bool tf32_narrow_n(const Problem& p, const Device& dev) {
 }
 
 uint64_t umma_workspace_bytes(const Problem& p, const Device& dev, bool tf32) {
-    const bool wide = p.k >= kWideMinK;
+    const bool wide = use_wide(p, dev, tf32);
     if (tf32) {
         if (tf32_narrow_n(p, dev)) return 0;   // 224-wide tiles: whole tiles only
         return wide ? workspace_bytes<true, true, true, 256>(p, dev) : workspace_bytes<true, true, false, 256>(p, dev);
@@ -675,7 +704,7 @@ uint64_t umma_workspace_bytes(const Problem& p, const Device& dev, bool tf32) {
 }
 
 cudaError_t launch_umma(const Problem& p, const Device& dev, bool tf32, void* workspace) {
-    const bool wide = p.k >= kWideMinK;
+    const bool wide = use_wide(p, dev, tf32);
     if (tf32) {
         if (tf32_narrow_n(p, dev))
             return wide ? launch<true, true, true, 224, false>(p, dev, nullptr)

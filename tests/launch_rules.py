@@ -1,0 +1,43 @@
+"""The tensor-core launcher's tile choices (csrc/umma.cu), restated for the tests.
+
+Tile height: 256-row ("wide") tiles when k >= 3072; for 1024 <= k < 3072
+where the wide grid needs no stream-K and fills its rounds of CTAs at least
+as well as the 128-row grid (a 128-row grid with stream-K counts as full);
+otherwise 128-row tiles.  Stream-K: the persistent plan has a region (T = qG
++ r tiles, q >= 1, r > 0, r * KT >= G) and whole tiles would fill less than
+3/4 of their CTA slots.
+"""
+
+
+def k_phases(k, mode):
+    """Phases of 128 bytes of k."""
+    return -(-k // (32 if mode == "tf32" else 64))
+
+
+def tiles_of(m, n, bm, bn=256):
+    return -(-m // bm) * -(-n // bn)
+
+
+def stream_k(tiles, kt, G=152):
+    r = tiles % G
+    waves = -(-tiles // G)
+    return tiles >= G and r > 0 and r * kt >= G and 4 * tiles < 3 * waves * G
+
+
+def slot_fill(m, n, bm, bn=256, G=152):
+    """Filled fraction of the CTA slots the whole-tile grid occupies."""
+    t = tiles_of(m, n, bm, bn)
+    return m * n / (-(-t // G) * G * bm * bn)
+
+
+def tile_rows(m, n, k, mode, G=152):
+    """256 or 128: the height of the tensor-core tiles the launcher picks."""
+    if k >= 3072:
+        return 256
+    if k < 1024:
+        return 128
+    kt = k_phases(k, mode)
+    if stream_k(tiles_of(m, n, 256), kt, G):
+        return 128
+    narrow = 1.0 if stream_k(tiles_of(m, n, 128), kt, G) else slot_fill(m, n, 128, G=G)
+    return 256 if slot_fill(m, n, 256, G=G) >= narrow else 128

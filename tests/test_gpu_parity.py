@@ -12,6 +12,7 @@ import torch
 import oracle
 from dense_tiled_matrix_gb300 import inputs, tgemm
 import parity
+import launch_rules
 
 pytestmark = pytest.mark.gpu
 
@@ -51,7 +52,7 @@ def test_edge_tiles(mode, shape):
                       f"{mode} uniform {shape}")
 
 
-# k >= 3072 takes the 256 x 256 tensor-core tiles; ragged m, n and k there too.
+# k >= 3072 always takes the 256 x 256 tensor-core tiles; ragged m, n and k there too.
 WIDE_SHAPES = [(300, 520, 3100), (257, 300, 4097), (129, 1000, 3072)]
 
 
@@ -61,6 +62,21 @@ def test_long_k_tiles(mode, shape):
     m, n, k = shape
     parity.full_check(mode, inputs.random_case(5000 + m + n + k, m, n, k, kind="int"), f"{mode} int {shape}")
     parity.full_check(mode, inputs.random_case(6000 + m + n + k, m, n, k, kind="uniform"), f"{mode} uniform {shape}")
+
+
+# 1024 <= k < 3072 where the 256-row tiles fill their rounds of CTAs at least
+# as well as the 128-row ones and need no stream-K: they take the 256 x 256
+# tiles too (one exact round of them; ragged m, n and k).
+MID_K_WIDE_SHAPES = [(2048, 4864, 1024), (2900, 5000, 1030)]
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+@pytest.mark.parametrize("shape", MID_K_WIDE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_mid_k_wide_tiles(mode, shape):
+    m, n, k = shape
+    assert launch_rules.tile_rows(m, n, k, mode) == 256
+    parity.full_check(mode, inputs.random_case(5100 + m + n + k, m, n, k, kind="int"), f"{mode} int {shape}")
+    parity.full_check(mode, inputs.random_case(6100 + m + n + k, m, n, k, kind="uniform"), f"{mode} uniform {shape}")
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -337,28 +353,27 @@ def test_ragged_right_edge_with_aligned_rows(mode, n):
     assert np.all(np.isnan(host[m:])), f"{mode}: wrote past row {m - 1}"
 
 
-# bf16 128-row tiles as multicast CTA pairs (k < 3072, no stream-K region, an
-# even number of tile rows and at least two rounds of tiles on GB300): whole
+# bf16 128-row tiles as multicast CTA pairs (128-row tiles, no stream-K region,
+# an even number of tile rows and at least two rounds of tiles on GB300): whole
 # output against the oracle, exact sizes, ragged m / n / k (the last tile row
 # partly empty) and short k.
-PAIR_SHAPES = [(2048, 4864, 1024), (2000, 4800, 999), (4096, 2432, 200)]
+PAIR_SHAPES = [(2048, 4864, 1000), (2000, 4800, 999), (4096, 2432, 200), (1536, 9728, 1024)]
 
 
 def takes_pairs(m, n, k, sms=152):
-    """The launcher's choice, restated: 128 x 256 tiles (k < 3072), no stream-K
-    (no region, or whole tiles filling at least 3/4 of their rounds), tile rows
-    in pairs, at least two rounds."""
-    tiles_m, tiles_n, kt = (m + 127) // 128, (n + 255) // 256, (k + 63) // 64
-    tiles = tiles_m * tiles_n
-    r = tiles % sms
-    region = tiles >= sms and r > 0 and r * kt >= sms
-    waves = (tiles + sms - 1) // sms
-    stream_k = region and 4 * tiles < 3 * waves * sms
-    return k < 3072 and not stream_k and tiles_m % 2 == 0 and tiles >= 2 * sms
+    """The launcher's choice, restated: 128 x 256 tiles (launch_rules.tile_rows),
+    no stream-K (no region, or whole tiles filling at least 3/4 of their
+    rounds), tile rows in pairs, at least two rounds."""
+    tiles_m = (m + 127) // 128
+    tiles = launch_rules.tiles_of(m, n, 128)
+    stream_k = launch_rules.stream_k(tiles, launch_rules.k_phases(k, "bf16"), sms)
+    return (launch_rules.tile_rows(m, n, k, "bf16", sms) == 128 and not stream_k and tiles_m % 2 == 0
+            and tiles >= 2 * sms)
 
 
 def test_pair_rule_restatement():
-    assert takes_pairs(8192, 8192, 2048) and takes_pairs(6144, 6144, 2048)
+    assert takes_pairs(2048, 4864, 1000) and takes_pairs(1536, 9728, 1024)
+    assert not takes_pairs(8192, 8192, 2048)        # 256-row tiles fill its rounds as well
     assert not takes_pairs(4097, 3001, 1023)        # 33 tile rows
     assert not takes_pairs(2560, 4352, 1024)        # stream-K: 340 tiles fill 75 % of 3 rounds
     assert not takes_pairs(8192, 8192, 8192)        # 256-row tiles
@@ -377,7 +392,7 @@ def test_bf16_cta_pairs_with_unaligned_c():
     """Pairs with C that TMA cannot describe (row pitch n + 1): the pair kernel
     with eight epilogue warps on the read-back path; NaN guard columns must
     stay untouched."""
-    m, n, k = 2048, 4864, 1024
+    m, n, k = 2048, 4864, 1000
     assert takes_pairs(m, n, k)
     case = inputs.random_case(8300, m, n, k, kind="int")
     A_np, B_np = parity.inputs_for("bf16", case)

@@ -25,6 +25,8 @@ tile's sum.
 import numpy as np
 import pytest
 
+import launch_rules
+
 BM, BN, BK = 128, 128, 16
 
 
@@ -206,31 +208,43 @@ def test_head_plus_tail_is_the_full_sum_on_integers():
 
 # ---- tcgen05 kernels (csrc/umma.cu): tile width, then the same plan ----
 def umma_choice(m, n, k, mode, G=152):
-    """(tile width, tiles, KT, stream-K) the launcher picks: 256 x BN tiles when
-    k >= 3072, else 128 x BN.  Stream-K (always with BN = 256) when the plan
-    has a region and whole tiles would fill less than 3/4 of the occupied CTA
-    slots; otherwise TF32 takes BN = 224 when that fills them better by more
-    than 2 %."""
-    bm = 256 if k >= 3072 else 128
-    kt = -(-k // (32 if mode == "tf32" else 64))
-
-    def fill(bn):
-        tiles = -(-m // bm) * -(-n // bn)
-        return m * n / (-(-tiles // G) * G * bm * bn), tiles
-
-    tiles = fill(256)[1]
-    waves = -(-tiles // G)
-    r = tiles % G
-    if tiles >= G and r > 0 and r * kt >= G and 4 * tiles < 3 * waves * G:
+    """(tile width, tiles, KT, stream-K) the launcher picks: 256 x BN or 128 x
+    BN tiles by the rule of launch_rules.tile_rows.  Stream-K (always with BN =
+    256) when the plan has a region and whole tiles would fill less than 3/4
+    of the occupied CTA slots; otherwise TF32 takes BN = 224 when that fills
+    them better by more than 2 %."""
+    bm = launch_rules.tile_rows(m, n, k, mode, G)
+    kt = launch_rules.k_phases(k, mode)
+    tiles = launch_rules.tiles_of(m, n, bm)
+    if launch_rules.stream_k(tiles, kt, G):
         return 256, tiles, kt, True
-    bn = 224 if mode == "tf32" and fill(224)[0] > 1.02 * fill(256)[0] else 256
-    return bn, fill(bn)[1], kt, False
+    fill = lambda bn: launch_rules.slot_fill(m, n, bm, bn, G)
+    bn = 224 if mode == "tf32" and fill(224) > 1.02 * fill(256) else 256
+    return bn, launch_rules.tiles_of(m, n, bm, bn), kt, False
 
 
 def test_umma_choices_on_the_benchmarked_shapes():
     assert umma_choice(4096, 4096, 4096, "tf32") == (224, 304, 128, False)   # 2 full waves
     assert umma_choice(8192, 8192, 8192, "bf16")[::3] == (256, False)        # 1024 tiles: 96 % filled
     assert umma_choice(4097, 3001, 1023, "tf32")[0] == 256
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+def test_umma_tile_rows_on_measured_shapes(mode):
+    """The tile-height rule on the shapes whose timings chose it: wide tiles at
+    long k, and at 1024 <= k < 3072 where their rounds are at least as full
+    (measured faster or equal); 128-row tiles where the wide rounds are
+    emptier (1536 x 9728 x 1024: 3/4 of two rounds against three full ones),
+    too few (2048^3: 64 wide tiles) or split (4097 x 3001 x 1023), and at k < 1024."""
+    for shape in [(8192, 8192, 8192), (8192, 8192, 1024), (2048, 4864, 1024), (2048, 4864, 2048),
+                  (3000, 6000, 1024), (2900, 5000, 1030), (4096, 4096, 2048), (6144, 3072, 1024)]:
+        assert launch_rules.tile_rows(*shape, mode) == 256, shape
+    for shape in [(1536, 9728, 1024), (2048, 2048, 2048), (4097, 3001, 1023), (2000, 2600, 1000),
+                  (8192, 8192, 1000), (2000, 4800, 999)]:
+        assert launch_rules.tile_rows(*shape, mode) == 128, shape
+    # the two grids' slot fills on the deciding shapes
+    assert launch_rules.slot_fill(1536, 9728, 256) == 0.75 and launch_rules.slot_fill(1536, 9728, 128) == 1.0
+    assert launch_rules.slot_fill(2900, 5000, 256) == launch_rules.slot_fill(2900, 5000, 128)
 
 
 @pytest.mark.parametrize("mode", ["tf32", "bf16"])
