@@ -201,7 +201,8 @@ def test_tf32_input_conversion(capsys):
 def _boundary_shapes(count, seed, budget=1.2e9):
     """Seeded shapes that sit near the dispatch boundaries: m around 64 (the
     skinny bf16 kernel), sizes around multiples of 64/128/224/256 (tile edges),
-    k around 2048 and 3072 (the tensor-core tile height switches at 3072) and
+    k around 1024, 2048 and 3072 (the tensor-core tiles are 256 rows high from
+    k = 3072, and from k = 1024 where those rounds fill as well) and
     tile counts around multiples of 152 (a partly empty last wave: split
     pieces, 224-wide tiles, stream-K)."""
     rng = np.random.default_rng(seed)
