@@ -14,7 +14,10 @@
 //    that fills better; visited by a persistent grid of one CTA per SM in
 //    groups of tile rows (neighbouring CTAs share A and B tiles in L2).  Where
 //    whole tiles would leave more than a quarter of the CTA slots idle, the
-//    last G + r tiles are split along k between CTAs (stream-K, stream_k.cuh).
+//    last G + r tiles are split along k between CTAs (stream-K, stream_k.cuh);
+//    where there are fewer tiles than SMs, every tile is cut along k into
+//    split-K pieces, one CTA each, whose partial sums a reduce kernel adds in
+//    piece order.
 //  * Phases of 128 bytes of K (64 bf16 or 32 fp32 elements).  Warp 0 streams
 //    the A tile (128 x BK, K-major) and the B tile into a 4-stage shared-memory
 //    ring with TMA, 128-byte swizzled so the tensor core reads them without
@@ -41,8 +44,9 @@
 //    reads the rows back and stores scalars, masked at the edges of C.
 //
 // Every C element is written exactly once.  The tensor cores add the k terms
-// in a fixed order, and a split tile is (head partial) + (tail partial), so
-// repeated runs are bit-identical.
+// in a fixed order, a stream-K tile is (head partial) + (tail partial) and a
+// split-K tile the sum of its pieces in piece order, so repeated runs are
+// bit-identical.
 #include <cstdio>
 #include <cstring>
 
@@ -122,7 +126,7 @@ __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
 umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
             const __grid_constant__ CUtensorMap tmC, float* __restrict__ C, int64_t ldc, int M, int N, int K,
             int vec_store, uint32_t* status,
-            float* __restrict__ ws, unsigned* __restrict__ flags) {
+            float* __restrict__ ws, unsigned* __restrict__ flags, int pieces) {
     using G = Cfg<kTF32, kBKMajor, kWide, kBN>;
     // kPair: the two CTAs of a (2 x 1) cluster take vertically adjacent 128 x 256
     // tiles, which use the same B tile: each loads half of its 128-byte chunks and
@@ -166,19 +170,35 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             tile_coords(unit, tiles_m, tiles_n, G::GROUP_M, tm, tn);
         }
     };
+    // kSK with pieces > 0: split-K pieces instead of the stream-K plan.  CTA u
+    // (one per unit) computes piece u % pieces of tile u / pieces, k-phases
+    // [KT p / pieces, KT (p + 1) / pieces), and stores its partial sums in
+    // workspace slot u; umma_pieces_reduce_kernel adds a tile's pieces in order.
+    const bool split = kSK && pieces > 0;
     SkPlan plan;
-    if (kSK) plan.init(tiles, KT, blockIdx.x, gridDim.x);
+    if (kSK && !split) plan.init(tiles, KT, blockIdx.x, gridDim.x);
     // The CTA's segments (tile, k-phases [ka, kz)): with kSK the plan's
-    // sequence, otherwise whole tiles b, b + G, ...  Each role walks its own.
+    // sequence or the CTA's one piece, otherwise whole tiles b, b + G, ...
+    // Each role walks its own.
     struct Seq {
         SkCursor cur;
         int t_next;
     };
     auto seq_init = [&](Seq& q) {
         q.t_next = unit0;
-        if (kSK) q.cur.init(plan);
+        if (kSK && !split) q.cur.init(plan);
     };
     auto seq_next = [&](Seq& q, int& t, int& ka, int& kz) -> bool {
+        if (split) {
+            if (q.t_next < 0) return false;
+            const int u = q.t_next;
+            q.t_next = -1;
+            t = u / pieces;
+            const int piece = u - t * pieces;
+            ka = static_cast<int>(static_cast<int64_t>(KT) * piece / pieces);
+            kz = static_cast<int>(static_cast<int64_t>(KT) * (piece + 1) / pieces);
+            return t < tiles;
+        }
         if (kSK) return q.cur.next(plan, KT, t, ka, kz);
         if (q.t_next >= units) return false;
         t = q.t_next;
@@ -361,7 +381,8 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             __syncwarp();   // tcgen05.ld below is warp-collective
             int tm, tn;
             coords(tile, tm, tn);
-            const bool tail = kSK && ka > 0;
+            // a piece stores its partial sums like a stream-K tail (no flag)
+            const bool tail = kSK && (split || ka > 0);
             const bool head = kSK && !tail && kz < KT;
             // Partial tile of a CTA's slot: float4 ((h * BN/32 + c) * 8 + q) * 128 + row
             // holds columns 32c + 4q .. +3 of row `row` of half h, so a warp
@@ -481,7 +502,7 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
             }
             tc_fence_before_sync();
             mbar_arrive(&acc_empty[acc]);
-            if (tail) {
+            if (tail && !split) {
                 __threadfence();
                 epilogue_sync<kEpiWarps>();
                 if (threadIdx.x == 64) st_release_u32(flags + blockIdx.x, 1u);
@@ -498,6 +519,50 @@ umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUt
         __syncwarp();
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, G::TMEM_COLS);
+    }
+}
+
+// C of split-K pieces: tile t is the sum of its pieces' partial sums (slots
+// t * pieces .. + pieces - 1), added in piece order, so repeated runs are
+// bit-identical.  A slot has the layout the kernel's epilogue writes: float4
+// ((h * BN/32 + c) * 8 + q) * 128 + r holds columns 32c + 4q .. +3 of row
+// 128h + r of the tile.  Block (t, j) takes float4s 1024 j .. +1023 of tile t,
+// so a warp reads 512 contiguous bytes of every slot.
+template <int BM, int BN, int kGroupM>
+__global__ void __launch_bounds__(256)
+umma_pieces_reduce_kernel(const float4* __restrict__ ws, float* __restrict__ C, int64_t ldc, int M, int N,
+                          int pieces, int vec_store) {
+    constexpr int kSlot4 = BM * BN / 4;
+    const int tiles_m = (M + BM - 1) / BM, tiles_n = (N + BN - 1) / BN;
+    const int t = static_cast<int>(blockIdx.x);
+    int tm, tn;
+    tile_coords(t, tiles_m, tiles_n, kGroupM, tm, tn);
+    const float4* src = ws + static_cast<int64_t>(t) * pieces * kSlot4;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int f = static_cast<int>(blockIdx.y) * 1024 + i * 256 + static_cast<int>(threadIdx.x);
+        if (f >= kSlot4) break;
+        float4 v = src[f];
+        for (int pc = 1; pc < pieces; ++pc) {
+            const float4 w = src[static_cast<int64_t>(pc) * kSlot4 + f];
+            v.x += w.x;
+            v.y += w.y;
+            v.z += w.z;
+            v.w += w.w;
+        }
+        const int g = f >> 7, q = g & 7, hc = g >> 3;
+        const int row = tm * BM + (hc / (BN / 32)) * 128 + (f & 127);
+        const int col = tn * BN + (hc % (BN / 32)) * 32 + q * 4;
+        if (row >= M) continue;
+        float* dst = C + static_cast<int64_t>(row) * ldc + col;
+        if (vec_store && col + 3 < N) {
+            *reinterpret_cast<float4*>(dst) = v;
+        } else {
+            const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (col + j < N) dst[j] = e[j];
+        }
     }
 }
 
@@ -523,17 +588,38 @@ bool has_sk(const Problem& p, const Device& dev) {
     return sk_has_region(tiles, (p.k + G::BK - 1) / G::BK, dev.sm_count) && 4 * tiles < 3 * waves * dev.sm_count;
 }
 
+// Split-K pieces where the whole tiles fill less than one round of CTAs (no
+// stream-K plan then): each tile is cut along k into P pieces, P = the most
+// that fit in one round with at least kMinPiecePhases k-phases each; the
+// pieces' partial sums are added by umma_pieces_reduce_kernel.
+constexpr int64_t kMinPiecePhases = 8;
+
+template <bool kTF32, bool kBKMajor, bool kWide, int kBN>
+int pieces_for(const Problem& p, const Device& dev) {
+    using G = Cfg<kTF32, kBKMajor, kWide, kBN>;
+    const int64_t tiles = tile_count<kTF32, kBKMajor, kWide, kBN>(p);
+    if (tiles <= 0 || tiles >= dev.sm_count) return 0;
+    const int64_t KT = (p.k + G::BK - 1) / G::BK;
+    int64_t pieces = dev.sm_count / tiles;
+    if (pieces > KT / kMinPiecePhases) pieces = KT / kMinPiecePhases;
+    return pieces >= 2 ? static_cast<int>(pieces) : 0;
+}
+
 template <bool kTF32, bool kBKMajor, bool kWide, int kBN>
 uint64_t workspace_bytes(const Problem& p, const Device& dev) {
     using G = Cfg<kTF32, kBKMajor, kWide, kBN>;
-    if (!has_sk<kTF32, kBKMajor, kWide, kBN>(p, dev)) return 0;
-    return static_cast<uint64_t>(dev.sm_count) * (static_cast<uint64_t>(G::BM) * G::BN * sizeof(float) +
-                                                  sizeof(unsigned));
+    const uint64_t slot = static_cast<uint64_t>(G::BM) * G::BN * sizeof(float);
+    if (has_sk<kTF32, kBKMajor, kWide, kBN>(p, dev))
+        return static_cast<uint64_t>(dev.sm_count) * (slot + sizeof(unsigned));   // a slot and a flag per CTA
+    const int pieces = pieces_for<kTF32, kBKMajor, kWide, kBN>(p, dev);
+    if (pieces > 0) return static_cast<uint64_t>(tile_count<kTF32, kBKMajor, kWide, kBN>(p)) * pieces * slot;
+    return 0;
 }
 
-// Stream-K (kSK, with its workspace) or whole tiles.
+// Stream-K (kSK, with its workspace), split-K pieces (kSK with pieces > 0,
+// then the reduce kernel) or whole tiles.
 template <bool kTF32, bool kBKMajor, bool kWide, int kBN, bool kSK, bool kPair = false>
-cudaError_t launch(const Problem& p, const Device& dev, void* workspace) {
+cudaError_t launch(const Problem& p, const Device& dev, void* workspace, int pieces = 0) {
     using G = Cfg<kTF32, kBKMajor, kWide, kBN>;
     const CUtensorMapDataType dt = kTF32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     CUtensorMap ta, tb;
@@ -596,11 +682,16 @@ cudaError_t launch(const Problem& p, const Device& dev, void* workspace) {
         attr[cfg.numAttrs].val.clusterDim.z = 1;
         ++cfg.numAttrs;
     }
-    if (kSK) {
-        if (!workspace) {
-            set_error("umma_kernel: stream-K form launched without its workspace");
-            return cudaErrorInvalidValue;
-        }
+    if (kSK && !workspace) {
+        set_error("umma_kernel: split form launched without its workspace");
+        return cudaErrorInvalidValue;
+    }
+    if (kSK && pieces > 0) {
+        // one CTA and one partial tile per piece; nothing waits on another CTA
+        ws = static_cast<float*>(workspace);
+        cfg.gridDim = dim3(static_cast<unsigned>(tiles * pieces), 1, 1);
+        cfg.numAttrs = 0;
+    } else if (kSK) {
         // one partial tile and one flag per CTA; the flags start cleared
         ws = static_cast<float*>(workspace);
         flags = reinterpret_cast<unsigned*>(ws + static_cast<size_t>(dev.sm_count) * G::BM * G::BN);
@@ -614,9 +705,23 @@ cudaError_t launch(const Problem& p, const Device& dev, void* workspace) {
         cfg.gridDim = dim3(static_cast<unsigned>(dev.sm_count), 1, 1);
         cfg.numAttrs = 1;
     }
-    err = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status, ws, flags);
+    err = cudaLaunchKernelEx(&cfg, kernel, ta, tb, tc, p.C, p.ldc, p.m, p.n, p.k, vec_store, dev.status, ws, flags,
+                             kSK ? pieces : 0);
     count_launch();
-    if (err != cudaSuccess) set_error("umma_kernel launch: %s", cudaGetErrorString(err));
+    if (err != cudaSuccess) {
+        set_error("umma_kernel launch: %s", cudaGetErrorString(err));
+        return err;
+    }
+    if constexpr (kSK) {
+        if (pieces <= 0) return err;
+        const int vec_c = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
+        const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>((G::BM * G::BN / 4 + 1023) / 1024), 1);
+        umma_pieces_reduce_kernel<G::BM, G::BN, G::GROUP_M><<<grid, 256, 0, p.stream>>>(
+            reinterpret_cast<const float4*>(ws), p.C, p.ldc, p.m, p.n, pieces, vec_c);
+        err = cudaGetLastError();
+        count_launch();
+        if (err != cudaSuccess) set_error("umma_pieces_reduce_kernel launch: %s", cudaGetErrorString(err));
+    }
     return err;
 }
 
@@ -624,6 +729,10 @@ template <bool kTF32, bool kBKMajor, bool kWide, int kBN>
 cudaError_t launch_any(const Problem& p, const Device& dev, void* workspace) {
     if (workspace && has_sk<kTF32, kBKMajor, kWide, kBN>(p, dev))
         return launch<kTF32, kBKMajor, kWide, kBN, true>(p, dev, workspace);
+    if (workspace) {
+        const int pieces = pieces_for<kTF32, kBKMajor, kWide, kBN>(p, dev);
+        if (pieces > 0) return launch<kTF32, kBKMajor, kWide, kBN, true>(p, dev, workspace, pieces);
+    }
     if constexpr (!kTF32 && !kBKMajor && !kWide) {
         // Pairs where the tile rows pair up evenly and fill at least two rounds.
         // Measured on GB300 (us per launch, single CTAs -> pairs): 8192 x 8192 x
@@ -685,6 +794,7 @@ bool use_wide(const Problem& p, const Device& dev, bool tf32) {
 bool tf32_narrow_n(const Problem& p, const Device& dev) {
     const bool wide = use_wide(p, dev, true);
     if (wide ? has_sk<true, true, true, 256>(p, dev) : has_sk<true, true, false, 256>(p, dev)) return false;
+    if (wide ? pieces_for<true, true, true, 256>(p, dev) : pieces_for<true, true, false, 256>(p, dev)) return false;
     const int64_t bm = wide ? 256 : 128, G = dev.sm_count;
     auto fill = [&](int64_t bn) {
         const int64_t tiles = ((p.m + bm - 1) / bm) * ((p.n + bn - 1) / bn);

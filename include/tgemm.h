@@ -22,8 +22,8 @@
  * library may take temporary stream-ordered workspace on `stream` (for
  * operands whose base address or leading dimension is not a multiple of 16
  * bytes, for B transposed on the TF32 path, and for the partial sums of
- * tiles that tgemm_f32 splits along k between several blocks) and returns it
- * on the same stream.
+ * tiles that a call splits along k between several blocks) and returns it on
+ * the same stream.
  *
  * Execution.  Every call is asynchronous on `stream` (NULL is the legacy
  * default stream) and returns once the work is queued.  Argument errors are
@@ -141,7 +141,8 @@ tgemm_status tgemm_transpose_f32(int64_t rows, int64_t cols,
  * codes as tgemm_tf32 (the pages have no counterpart: this concerns only where
  * the library keeps its temporary data).  It never splits an output tile along
  * k between CTAs, so on shapes where tgemm_tf32 does (a partly filled last
- * wave of tiles) the k terms are added in another order: the results agree
+ * wave of tiles, or fewer tiles than SMs) the k terms are added in another
+ * order: the results agree
  * with tgemm_tf32 within the TF32 error bound, exactly on integer-valued
  * inputs, and may take longer there.
  *

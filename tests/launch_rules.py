@@ -5,7 +5,7 @@ where the wide grid needs no stream-K and fills its rounds of CTAs at least
 as well as the 128-row grid (a 128-row grid with stream-K counts as full);
 otherwise 128-row tiles.  Stream-K: the persistent plan has a region (T = qG
 + r tiles, q >= 1, r > 0, r * KT >= G) and whole tiles would fill less than
-3/4 of their CTA slots.
+3/4 of their CTA slots.  Split-K pieces: fewer tiles than CTAs (see pieces).
 """
 
 
@@ -41,3 +41,15 @@ def tile_rows(m, n, k, mode, G=152):
         return 128
     narrow = 1.0 if stream_k(tiles_of(m, n, 128), kt, G) else slot_fill(m, n, 128, G=G)
     return 256 if slot_fill(m, n, 256, G=G) >= narrow else 128
+
+
+def pieces(m, n, k, mode, G=152):
+    """Split-K pieces per tile (0: none): where the whole tiles (of the height
+    tile_rows picks, 256 wide) fill less than one round of CTAs, each tile is
+    cut along k into as many pieces as fit in one round, each at least 8
+    k-phases long; at least 2."""
+    tiles = tiles_of(m, n, tile_rows(m, n, k, mode, G))
+    if tiles >= G:
+        return 0
+    p = min(G // tiles, k_phases(k, mode) // 8)
+    return p if p >= 2 else 0

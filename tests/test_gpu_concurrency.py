@@ -3,8 +3,8 @@
 The library keeps no per-call state outside the call: the error text is
 thread-local, the device table is set up once under a lock, and every
 workspace (re-pitched operands, the TF32 B transpose, fp32 k-pieces,
-tensor-core stream-K partials) is stream-ordered memory of the calling
-stream.  So concurrent calls on different streams must give the same
+tensor-core stream-K and split-K partials) is stream-ordered memory of the
+calling stream.  So concurrent calls on different streams must give the same
 results as calls one at a time: here every result must equal the oracle
 exactly (integer inputs) while four threads run all the workspace-using
 paths at the same time.  (`tgemm_tf32_noalloc` shares one static scratch
@@ -27,6 +27,7 @@ CASES = [
     ("f32", (1025, 700, 301)),      # misaligned rows: re-pitch (workspace)
     ("tf32", (300, 520, 200)),      # B transpose (workspace)
     ("bf16", (2000, 2600, 1000)),   # tensor-core stream-K (workspace)
+    ("tf32", (300, 520, 3100)),     # split-K pieces + reduce (workspace)
     ("bf16", (16, 1000, 4100)),     # skinny cluster split
     ("bf16", (257, 511, 257)),      # whole tiles, ragged edges
     ("bf16", (2048, 4864, 1000)),   # multicast CTA pairs (cluster launches)

@@ -14,7 +14,8 @@ Multiplication Kernel", the two __syncthreads: no thread reads a tile before
 it is loaded, none overwrites a tile still in use).
 
 Every kernel path runs here on small and edge cases, ragged tiles, split tiles
-(fp32 k-pieces, tensor-core stream-K, skinny split tiles) and re-pitched
+(fp32 k-pieces, tensor-core stream-K and split-K pieces, skinny split
+tiles) and re-pitched
 operands; each output must match the oracle (exactly on integer inputs) and
 the status word must stay clear.  The reporting path itself is exercised with
 tgemm_selftest_debug_check, which records a failed check without any other
@@ -65,7 +66,8 @@ CASES = [
     ((129, 257, 17), ["f32", "tf32", "bf16"]),
     ((1000, 64, 65), ["f32", "tf32", "bf16"]),
     ((257, 511, 257), ["f32", "tf32", "bf16"]),
-    ((300, 520, 3100), ["f32", "tf32", "bf16"]),        # 256 x 256 tensor-core tiles
+    ((300, 520, 3100), ["f32", "tf32", "bf16"]),        # 256 x 256 tensor-core tiles as split-K pieces
+    ((1000, 1001, 2000), ["tf32", "bf16"]),               # 128 x 256 tiles as split-K pieces, C unaligned
     ((1000, 900, 4100), ["f32"]),                         # fp32 k-pieces + ordered reduce
     ((3300, 3000, 3100), ["tf32", "bf16"]),               # tensor-core stream-K
     ((2000, 2600, 1000), ["tf32", "bf16"]),               # stream-K with 128 x 256 tiles

@@ -52,7 +52,8 @@ def test_edge_tiles(mode, shape):
                       f"{mode} uniform {shape}")
 
 
-# k >= 3072 always takes the 256 x 256 tensor-core tiles; ragged m, n and k there too.
+# k >= 3072 always takes the 256 x 256 tensor-core tiles; ragged m, n and k there
+# too (these few tiles run as split-K pieces).
 WIDE_SHAPES = [(300, 520, 3100), (257, 300, 4097), (129, 1000, 3072)]
 
 
@@ -404,6 +405,47 @@ def test_bf16_cta_pairs_with_unaligned_c():
     torch.cuda.synchronize()
     P, D = oracle.gemm(A_np, B_np)
     parity.check("bf16", C.cpu().numpy(), P, D, True, "bf16 pairs, unaligned C")
+    host = C_buf[: m * ldc].view(m, ldc).cpu().numpy()
+    assert np.all(np.isnan(host[:, n:])), "wrote past column n - 1"
+    assert np.all(np.isnan(C_buf[m * ldc:].cpu().numpy()))
+
+
+# Fewer tensor-core tiles than SMs with long k: each tile is cut along k into
+# split-K pieces (one CTA each, partial sums in the workspace) that the reduce
+# kernel adds in piece order.  256-row and 128-row tiles, ragged edges, m just
+# above the skinny kernel's 64 rows.  Whole output against the oracle, and
+# repeated runs bit-identical.
+PIECE_SHAPES = [(1024, 1024, 8192), (65, 4096, 4096), (1000, 1001, 2000), (129, 1000, 3072)]
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+@pytest.mark.parametrize("shape", PIECE_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_split_k_pieces(mode, shape):
+    m, n, k = shape
+    assert launch_rules.pieces(m, n, k, mode) >= 2
+    parity.full_check(mode, inputs.random_case(8400 + m + n + k, m, n, k, kind="int"), f"{mode} pieces int {shape}")
+    case = inputs.random_case(8500 + m + n + k, m, n, k, kind="uniform")
+    parity.full_check(mode, case, f"{mode} pieces uniform {shape}")
+    A, B = parity.inputs_for(mode, case)
+    A, B = parity.to_device(A), parity.to_device(B)
+    assert torch.equal(parity.ENTRY[mode](A, B), parity.ENTRY[mode](A, B))
+
+
+@pytest.mark.parametrize("mode", ["tf32", "bf16"])
+def test_split_k_pieces_with_unaligned_c(mode):
+    """Pieces with C rows that are not 16-byte aligned (row pitch n + 1): the
+    reduce kernel's scalar stores; NaN guard columns must stay untouched."""
+    m, n, k = 1000, 1001, 2000
+    assert launch_rules.pieces(m, n, k, mode) >= 2
+    case = inputs.random_case(8600, m, n, k, kind="int")
+    A_np, B_np = parity.inputs_for(mode, case)
+    ldc = n + 1
+    C_buf = torch.full((m * ldc + 8,), float("nan"), device="cuda")
+    C = C_buf[: m * ldc].view(m, ldc)[:, :n]
+    parity.ENTRY[mode](parity.to_device(A_np), parity.to_device(B_np), C)
+    torch.cuda.synchronize()
+    P, D = oracle.gemm(A_np, B_np)
+    parity.check(mode, C.cpu().numpy(), P, D, True, f"{mode} pieces, unaligned C")
     host = C_buf[: m * ldc].view(m, ldc).cpu().numpy()
     assert np.all(np.isnan(host[:, n:])), "wrote past column n - 1"
     assert np.all(np.isnan(C_buf[m * ldc:].cpu().numpy()))

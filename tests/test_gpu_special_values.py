@@ -8,7 +8,7 @@ M(i, k), or NaN where M(i, k) = 0 (0 * inf), and every other entry stays the
 exact integer sum.  Split sums must keep this: the special values are placed
 in the first and last k steps and in ragged edge columns, so that they sit in
 different k-slices of the fp32 k-pieces, the tensor-core stream-K halves and
-the skinny kernel's cluster ranks, and in partial tiles.
+split-K pieces and the skinny kernel's cluster ranks, and in partial tiles.
 """
 import numpy as np
 import pytest
@@ -49,6 +49,7 @@ CASES = [
     ((129, 257, 17), ["f32", "tf32", "bf16"]),        # ragged tiles everywhere
     ((1000, 900, 4100), ["f32"]),                      # fp32 k-pieces + ordered reduce
     ((2000, 2600, 1000), ["tf32", "bf16"]),            # tensor-core stream-K
+    ((300, 520, 3100), ["tf32", "bf16"]),              # tensor-core split-K pieces
     ((16, 1000, 4100), ["bf16"]),                      # skinny, k split over a cluster
     ((33, 129, 70), ["bf16"]),                         # skinny 64-row form, ragged
 ]

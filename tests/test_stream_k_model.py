@@ -247,6 +247,48 @@ def test_umma_tile_rows_on_measured_shapes(mode):
     assert launch_rules.slot_fill(2900, 5000, 256) == launch_rules.slot_fill(2900, 5000, 128)
 
 
+def test_umma_pieces_choices():
+    """Split-K pieces where the tiles fill less than one round: as many pieces
+    as fit in the round, each at least 8 k-phases; none at a round or more,
+    nor where pieces would be shorter."""
+    P = launch_rules.pieces
+    assert P(1024, 1024, 8192, "bf16") == 9 and P(1024, 1024, 8192, "tf32") == 9   # 16 wide tiles
+    assert P(256, 256, 65536, "bf16") == 128 and P(256, 256, 65536, "tf32") == 152  # one tile
+    assert P(300, 520, 3100, "bf16") == 6                                          # 6 tiles, 49 phases
+    assert P(65, 4096, 4096, "bf16") == 8                                          # 16 tiles, 64 phases
+    assert P(1000, 1001, 2000, "bf16") == 4                                        # 32 128-row tiles
+    assert P(2048, 2048, 1024, "bf16") == 0          # 128 tiles: 152 // 128 = 1
+    assert P(4096, 4096, 4096, "bf16") == 0          # a full round and more
+    assert P(1024, 1024, 512, "bf16") == 0           # 8 phases: no two pieces of 8
+    assert P(1024, 1024, 512, "tf32") == 2           # 16 TF32 phases
+
+
+@pytest.mark.parametrize("shape", [(1024, 1024, 8192), (300, 520, 3100), (256, 256, 65536), (1000, 1001, 2000)])
+def test_umma_pieces_cover_k_once_and_sum_exactly(shape):
+    """Piece p of a tile takes k-phases [KT p / P, KT (p + 1) / P): together they
+    cover every phase once, none is empty, and their partial sums added in
+    piece order give the tile's sum exactly on integers."""
+    m, n, k = shape
+    for mode in ("bf16", "tf32"):
+        pc = launch_rules.pieces(m, n, k, mode)
+        kt = launch_rules.k_phases(k, mode)
+        ranges = [(kt * p // pc, kt * (p + 1) // pc) for p in range(pc)]
+        assert ranges[0][0] == 0 and ranges[-1][1] == kt
+        assert all(a < b and b - a >= 8 for a, b in ranges)
+        assert all(ranges[i][1] == ranges[i + 1][0] for i in range(pc - 1))
+    rng = np.random.default_rng(7)
+    bk = 64
+    A = rng.integers(-3, 4, (16, k)).astype(np.float32)
+    B = rng.integers(-3, 4, (k, 8)).astype(np.float32)
+    kt = launch_rules.k_phases(k, "bf16")
+    pc = launch_rules.pieces(m, n, k, "bf16")
+    C = np.zeros((16, 8), np.float32)
+    for p in range(pc):
+        a, b = kt * p // pc * bk, min(k, kt * (p + 1) // pc * bk)
+        C += A[:, a:b] @ B[a:b]
+    np.testing.assert_array_equal(C, A @ B)
+
+
 @pytest.mark.parametrize("mode", ["tf32", "bf16"])
 def test_umma_stream_k_shapes(mode):
     G = 152
