@@ -14,7 +14,8 @@ which penalises memory-bound kernels for work they did not do.)
 
 The same JSON line carries, for information, the other measured shapes
 (4096^3 on the TF32 tensor-core path, 16 x 8192 x 8192 bf16, the
-4097 x 3001 x 1023 fp32 edge-tile case), a roofline object for the kernel
+4097 x 3001 x 1023 edge-tile case, 1024 x 1024 x 8192 on tensor-core split-K
+pieces, the pages' kernels), a roofline object for the kernel
 taking most of the step's time, the end-to-end number through the C ABI from
 pinned host buffers (every step copies its inputs in and its results out; the
 copies run on their own streams beside the products, and the same step with
@@ -81,6 +82,9 @@ EXTRAS = {
     "irregular_f32": ("irregular", "f32", "f32"),
     "irregular_tf32": ("irregular", "tf32", "f32"),
     "irregular_bf16": ("irregular", "bf16", "bf16"),
+    # fewer tensor-core tiles than SMs: split-K pieces and their reduce
+    "long_k_tf32": ("long_k", "tf32", "f32"),
+    "long_k_bf16": ("long_k", "bf16", "bf16"),
     # the pages' own experiment (naive -> tiled -> libtgemm) at 1024^3 and 4096^3
     "f32_1024": ("int1024", "f32", "f32"),
     "pages_naive_1024": ("int1024", "pages_naive", "f32"),

@@ -27,6 +27,7 @@ Workloads (seed 1000 + c for workload c; M is stream 0, N is stream 1)
     bf16_8192   : 8192^3 bf16, N(0, 1) / sqrt(8192)
     irregular   : 4097 x 3001 x 1023, uniform [-1, 1], lda = 1023, ldb = 3001
     skinny      : 16 x 8192 x 8192 bf16, uniform [-1, 1]
+    long_k      : 1024 x 1024 x 8192, uniform [-1, 1] (fewer output tiles than SMs)
 """
 from __future__ import annotations
 
@@ -199,6 +200,8 @@ def make(name: str, dtype: str | None = None) -> Case:
     elif name == "skinny":
         c = Case(name, to_bf16_bits(uniform_pm1(1004, 2, (16, 8192))),
                  to_bf16_bits(uniform_pm1(1004, 3, (8192, 8192))), "bf16")
+    elif name == "long_k":
+        c = Case(name, uniform_pm1(1005, 0, (1024, 8192)), uniform_pm1(1005, 1, (8192, 1024)), "f32")
     else:
         raise KeyError(f"unknown workload {name!r}")
     if dtype is not None and dtype != c.dtype:
