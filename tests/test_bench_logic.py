@@ -103,3 +103,24 @@ def test_clock_log_reports_every_throttle_reason_seen(tmp_path):
 def test_clock_log_without_samples(tmp_path):
     out = _summary(tmp_path, [""])
     assert out["reasons"] == ["no samples"] and out["sm_mhz"] is None
+
+
+def test_every_bench_shape_names_a_workload_and_an_entry():
+    """Each part of the step and each extra shape names a seeded workload that
+    inputs.make builds (sizes as the bench docstring states them) and an entry
+    point the bench knows; the two split-K extras have fewer tensor-core tiles
+    than SMs."""
+    from dense_tiled_matrix_gb300 import inputs
+    import launch_rules
+    entries = {"f32", "tf32", "bf16", "pages_naive", "pages_tiled16", "pages_tiled32"}
+    sizes = {}
+    for name, (wl, entry, _) in list(bench.PARTS.items()) + list(bench.EXTRAS.items()):
+        assert entry in entries, name
+        if wl not in sizes:
+            c = inputs.make(wl)
+            sizes[wl] = (c.m, c.n, c.k)
+    assert sizes["bf16_8192"] == (8192, 8192, 8192) and sizes["n4096"] == (4096, 4096, 4096)
+    assert sizes["skinny"] == (16, 8192, 8192) and sizes["irregular"] == (4097, 3001, 1023)
+    assert sizes["long_k"] == (1024, 1024, 8192)
+    for mode in ("bf16", "tf32"):
+        assert launch_rules.pieces(*sizes["long_k"], mode) >= 2
