@@ -82,10 +82,14 @@ cudaError_t launch_ffma_f32(const Problem& p, const Device& dev, void* workspace
 // inputs, and then p.B must hold B TRANSPOSED (n x k, pitch p.ldb, k
 // contiguous); otherwise bf16 inputs under kind::f16 with B as k x n.  With
 // umma_workspace_bytes() of stream-ordered workspace (no initial contents)
-// the last partial wave of tiles is split along k (stream-K); with nullptr
-// whole tiles only.
+// the last partial wave of tiles is split along k (stream-K), or, with fewer
+// tiles than SMs, every tile (split-K pieces); with nullptr whole tiles only.
 uint64_t umma_workspace_bytes(const Problem& p, const Device& dev, bool tf32);
 cudaError_t launch_umma(const Problem& p, const Device& dev, bool tf32, void* workspace);
+// The tiles launch_umma would use (host arithmetic only, only dev.sm_count read):
+// out[0] tile rows, out[1] tile columns, out[2] stream-K, out[3] split-K pieces
+// per tile, out[4] multicast CTA pairs.
+void umma_plan(const Problem& p, const Device& dev, bool tf32, bool workspace, int out[5]);
 
 // bf16 tcgen05 kernel for m <= 64: C^T = B^T A^T with k split across the CTAs
 // of a cluster and the partials added through distributed shared memory.

@@ -447,6 +447,24 @@ tgemm_status tgemm_get_device_status(struct CUstream_st* stream) {
 
 uint64_t tgemm_kernel_launches(void) { return tgemm::g_launches.load(std::memory_order_relaxed); }
 
+tgemm_status tgemm_plan(int tf32, int64_t m, int64_t n, int64_t k, int sm_count, int workspace, int* out) {
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (!out || m < 1 || n < 1 || k < 1 || m > lim || n > lim || k > lim || sm_count < 1 || sm_count > 4096)
+        return TGEMM_ERR_INVALID_VALUE;
+    int plan[5] = {0, 0, 0, 0, 0};
+    if (tf32 || m > 64) {   // bf16 with m <= 64 takes the skinny kernel: all zero
+        tgemm::Problem p;
+        p.m = static_cast<int>(m);
+        p.n = static_cast<int>(n);
+        p.k = static_cast<int>(k);
+        tgemm::Device d;
+        d.sm_count = sm_count;
+        tgemm::umma_plan(p, d, tf32 != 0, workspace != 0, plan);
+    }
+    for (int i = 0; i < 5; ++i) out[i] = plan[i];
+    return TGEMM_OK;
+}
+
 int tgemm_version(void) { return 200; }
 
 int tgemm_debug_build(void) { return tgemm::kDebugBuild ? 1 : 0; }

@@ -725,6 +725,17 @@ cudaError_t launch(const Problem& p, const Device& dev, void* workspace, int pie
     return err;
 }
 
+// Pairs where the tile rows pair up evenly and fill at least two rounds (bf16
+// 128 x 256 whole tiles).  Measured on GB300 (us per launch, single CTAs ->
+// pairs): 8192 x 8192 x 2048 201.4 -> 194.6, 8192 x 8192 x 1024 120.6 -> 116.3,
+// 6144 x 6144 x 2048 113.8 -> 110.8, 3000 x 6000 x 1024 39.8 -> 39.3; but 4097 x
+// 3001 x 1023 (33 tile rows: one pair half empty) 50.3 -> 57.2 and 1000 x 1001 x
+// 999 (32 tiles) 27.3 -> 28.6.
+bool use_pairs(const Problem& p, const Device& dev) {
+    const int64_t tiles_m = (p.m + 127) / 128;
+    return kUsePairs && tiles_m % 2 == 0 && tile_count<false, false, false, 256>(p) >= 2 * dev.sm_count;
+}
+
 template <bool kTF32, bool kBKMajor, bool kWide, int kBN>
 cudaError_t launch_any(const Problem& p, const Device& dev, void* workspace) {
     if (workspace && has_sk<kTF32, kBKMajor, kWide, kBN>(p, dev))
@@ -733,16 +744,8 @@ cudaError_t launch_any(const Problem& p, const Device& dev, void* workspace) {
         const int pieces = pieces_for<kTF32, kBKMajor, kWide, kBN>(p, dev);
         if (pieces > 0) return launch<kTF32, kBKMajor, kWide, kBN, true>(p, dev, workspace, pieces);
     }
-    if constexpr (!kTF32 && !kBKMajor && !kWide) {
-        // Pairs where the tile rows pair up evenly and fill at least two rounds.
-        // Measured on GB300 (us per launch, single CTAs -> pairs): 8192 x 8192 x
-        // 2048 201.4 -> 194.6, 8192 x 8192 x 1024 120.6 -> 116.3, 6144 x 6144 x
-        // 2048 113.8 -> 110.8, 3000 x 6000 x 1024 39.8 -> 39.3; but 4097 x 3001 x
-        // 1023 (33 tile rows: one pair half empty) 50.3 -> 57.2 and 1000 x 1001 x
-        // 999 (32 tiles) 27.3 -> 28.6.
-        const int64_t tiles_m = (p.m + 127) / 128;
-        if (kUsePairs && tiles_m % 2 == 0 && tile_count<kTF32, kBKMajor, kWide, kBN>(p) >= 2 * dev.sm_count)
-            return launch<kTF32, kBKMajor, kWide, kBN, false, true>(p, dev, nullptr);
+    if constexpr (!kTF32 && !kBKMajor && !kWide && kBN == 256) {
+        if (use_pairs(p, dev)) return launch<kTF32, kBKMajor, kWide, kBN, false, true>(p, dev, nullptr);
     }
     return launch<kTF32, kBKMajor, kWide, kBN, false>(p, dev, nullptr);
 }
@@ -811,6 +814,32 @@ uint64_t umma_workspace_bytes(const Problem& p, const Device& dev, bool tf32) {
         return wide ? workspace_bytes<true, true, true, 256>(p, dev) : workspace_bytes<true, true, false, 256>(p, dev);
     }
     return wide ? workspace_bytes<false, false, true, 256>(p, dev) : workspace_bytes<false, false, false, 256>(p, dev);
+}
+
+// The choice launch_umma makes, without launching (see tgemm_plan).
+void umma_plan(const Problem& p, const Device& dev, bool tf32, bool workspace, int out[5]) {
+    const bool wide = use_wide(p, dev, tf32);
+    out[0] = wide ? 256 : 128;
+    out[1] = 256;
+    out[2] = out[3] = out[4] = 0;
+    if (tf32 && tf32_narrow_n(p, dev)) {
+        out[1] = 224;
+        return;
+    }
+    const bool sk = tf32 ? (wide ? has_sk<true, true, true, 256>(p, dev) : has_sk<true, true, false, 256>(p, dev))
+                         : (wide ? has_sk<false, false, true, 256>(p, dev) : has_sk<false, false, false, 256>(p, dev));
+    if (workspace && sk) {
+        out[2] = 1;
+        return;
+    }
+    const int pieces = tf32 ? (wide ? pieces_for<true, true, true, 256>(p, dev) : pieces_for<true, true, false, 256>(p, dev))
+                            : (wide ? pieces_for<false, false, true, 256>(p, dev)
+                                    : pieces_for<false, false, false, 256>(p, dev));
+    if (workspace && pieces > 0) {
+        out[3] = pieces;
+        return;
+    }
+    if (!tf32 && !wide && use_pairs(p, dev)) out[4] = 1;
 }
 
 cudaError_t launch_umma(const Problem& p, const Device& dev, bool tf32, void* workspace) {

@@ -43,6 +43,8 @@ SIGNATURES = {
     "tgemm_selftest_debug_check": (ctypes.c_int, [_VP]),
     "tgemm_debug_build": (ctypes.c_int, []),
     "tgemm_kernel_launches": (ctypes.c_uint64, []),
+    "tgemm_plan": (ctypes.c_int, [ctypes.c_int, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
+                                  ctypes.POINTER(ctypes.c_int)]),
     "tgemm_version": (ctypes.c_int, []),
 }
 
@@ -200,6 +202,16 @@ def tgemm_kernel_launches() -> int:
 
 def tgemm_version() -> int:
     return int(load().tgemm_version())
+
+
+def tgemm_plan(mode: str, m: int, n: int, k: int, sm_count: int = 152, workspace: bool = True) -> dict:
+    """The tensor-core tiles tgemm_tf32 (mode "tf32") or tgemm_bf16 (mode
+    "bf16") would use; see tgemm_plan in include/tgemm.h."""
+    out = (ctypes.c_int * 5)()
+    st = load().tgemm_plan(1 if mode == "tf32" else 0, m, n, k, sm_count, 1 if workspace else 0, out)
+    _check(st)
+    return {"tile_rows": out[0], "tile_cols": out[1], "stream_k": bool(out[2]), "pieces": out[3],
+            "pairs": bool(out[4])}
 
 
 def raw(name: str):

@@ -212,6 +212,18 @@ int tgemm_debug_build(void);
 /* Kernels launched by this library in this process so far (all devices). */
 uint64_t tgemm_kernel_launches(void);
 
+/* The tensor-core tiles tgemm_tf32 (tf32 != 0) or tgemm_bf16 would use for an
+ * m x n x k product on a GPU with sm_count SMs: with the workspace those calls
+ * take (workspace != 0), or without it, as tgemm_tf32_noalloc.  Host arithmetic
+ * only: no CUDA call, no device needed.  Writes out[0] = tile rows (128 or
+ * 256), out[1] = tile columns (256 or 224), out[2] = 1 where the last tiles
+ * are split along k between two CTAs (stream-K), out[3] = split-K pieces per
+ * tile (0: none), out[4] = 1 for multicast CTA pairs; all five are 0 for bf16
+ * with m <= 64, which takes the cluster split-K kernel instead.  Returns
+ * TGEMM_OK, or TGEMM_ERR_INVALID_VALUE (out untouched) for a NULL out, sizes
+ * outside 1 .. 2^31 - 1 or sm_count outside 1 .. 4096. */
+tgemm_status tgemm_plan(int tf32, int64_t m, int64_t n, int64_t k, int sm_count, int workspace, int *out);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int tgemm_version(void);
 

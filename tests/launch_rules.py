@@ -53,3 +53,41 @@ def pieces(m, n, k, mode, G=152):
         return 0
     p = min(G // tiles, k_phases(k, mode) // 8)
     return p if p >= 2 else 0
+
+
+def tile_cols(m, n, k, mode, G=152):
+    """256, or 224 for TF32 where the whole tiles take neither stream-K nor
+    pieces and 224-wide ones fill the occupied CTA slots better by more than 2 %."""
+    if mode != "tf32":
+        return 256
+    bm = tile_rows(m, n, k, mode, G)
+    if stream_k(tiles_of(m, n, bm), k_phases(k, mode), G) or pieces(m, n, k, mode, G):
+        return 256
+    return 224 if slot_fill(m, n, bm, 224, G) > 1.02 * slot_fill(m, n, bm, 256, G) else 256
+
+
+def pairs(m, n, k, G=152):
+    """bf16 128 x 256 whole tiles as multicast CTA pairs: no stream-K, no pieces,
+    an even number of tile rows and at least two rounds of tiles."""
+    if tile_rows(m, n, k, "bf16", G) != 128:
+        return False
+    tiles = tiles_of(m, n, 128)
+    if stream_k(tiles, k_phases(k, "bf16"), G) or pieces(m, n, k, "bf16", G):
+        return False
+    return (-(-m // 128)) % 2 == 0 and tiles >= 2 * G
+
+
+def plan(m, n, k, mode, G=152, workspace=True):
+    """(tile rows, tile columns, stream-K, pieces, pairs) as tgemm_plan reports
+    them; bf16 with m <= 64 (the cluster split-K kernel) is all zero.  Without
+    workspace neither stream-K nor pieces is taken."""
+    if mode == "bf16" and m <= 64:
+        return (0, 0, False, 0, False)
+    bm, bn = tile_rows(m, n, k, mode, G), tile_cols(m, n, k, mode, G)
+    if bn == 224:
+        return (bm, 224, False, 0, False)
+    sk = workspace and stream_k(tiles_of(m, n, bm), k_phases(k, mode), G)
+    pc = pieces(m, n, k, mode, G) if workspace and not sk else 0
+    pr = mode == "bf16" and not sk and not pc and bm == 128 and (-(-m // 128)) % 2 == 0 \
+        and tiles_of(m, n, 128) >= 2 * G
+    return (bm, bn, sk, pc, pr)

@@ -363,14 +363,11 @@ PAIR_SHAPES = [(2048, 4864, 1000), (2000, 4800, 999), (4096, 2432, 200), (1536, 
 
 
 def takes_pairs(m, n, k, sms=152):
-    """The launcher's choice, restated: 128 x 256 tiles (launch_rules.tile_rows),
-    no stream-K (no region, or whole tiles filling at least 3/4 of their
-    rounds), tile rows in pairs, at least two rounds."""
-    tiles_m = (m + 127) // 128
-    tiles = launch_rules.tiles_of(m, n, 128)
-    stream_k = launch_rules.stream_k(tiles, launch_rules.k_phases(k, "bf16"), sms)
-    return (launch_rules.tile_rows(m, n, k, "bf16", sms) == 128 and not stream_k and tiles_m % 2 == 0
-            and tiles >= 2 * sms)
+    """The launcher's choice, restated (launch_rules.pairs) and checked against
+    the library's own plan (tgemm_plan)."""
+    want = launch_rules.pairs(m, n, k, sms)
+    assert tgemm.tgemm_plan("bf16", m, n, k, sms)["pairs"] == want
+    return want
 
 
 def test_pair_rule_restatement():
