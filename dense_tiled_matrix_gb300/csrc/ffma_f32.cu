@@ -534,6 +534,18 @@ uint64_t ffma_f32_workspace_bytes(const Problem& p, const Device& dev) {
     return static_cast<uint64_t>(st.rest) * st.parts * FCfg::BM * kBN * sizeof(float);
 }
 
+void ffma_f32_plan(const Problem& p, const Device& dev, int64_t out[3]) {
+    SplitTail st;
+    if (split_tail(p, dev, &st)) {
+        out[0] = st.full;
+        out[1] = st.rest;
+        out[2] = st.parts;
+        return;
+    }
+    out[0] = static_cast<int64_t>((p.m + FCfg::BM - 1) / FCfg::BM) * ((p.n + kBN - 1) / kBN);
+    out[1] = out[2] = 0;
+}
+
 cudaError_t launch_ffma_f32(const Problem& p, const Device& dev, void* workspace) {
     SplitTail st;
     return split_tail(p, dev, &st) ? launch_split_tail(p, dev, workspace, st) : launch_tiles(p, dev);

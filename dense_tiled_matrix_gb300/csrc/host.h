@@ -77,6 +77,10 @@ inline bool sk_has_region(int64_t tiles, int64_t KT, int64_t G) {
 // until the kernel has run; others need none and take nullptr.
 uint64_t ffma_f32_workspace_bytes(const Problem& p, const Device& dev);
 cudaError_t launch_ffma_f32(const Problem& p, const Device& dev, void* workspace);
+// The tiles launch_ffma_f32 would run (host arithmetic only, only dev.sm_count
+// read): out[0] whole tiles, out[1] remainder tiles cut along k, out[2] pieces
+// per remainder tile (0: none).
+void ffma_f32_plan(const Problem& p, const Device& dev, int64_t out[3]);
 
 // tcgen05 kernels; same alignment rule.  `tf32` selects kind::tf32 on fp32
 // inputs, and then p.B must hold B TRANSPOSED (n x k, pitch p.ldb, k

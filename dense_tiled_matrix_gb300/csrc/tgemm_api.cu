@@ -465,6 +465,22 @@ tgemm_status tgemm_plan(int tf32, int64_t m, int64_t n, int64_t k, int sm_count,
     return TGEMM_OK;
 }
 
+tgemm_status tgemm_plan_f32(int64_t m, int64_t n, int64_t k, int sm_count, int64_t* out) {
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (!out || m < 1 || n < 1 || k < 1 || m > lim || n > lim || k > lim || sm_count < 1 || sm_count > 4096)
+        return TGEMM_ERR_INVALID_VALUE;
+    tgemm::Problem p;
+    p.m = static_cast<int>(m);
+    p.n = static_cast<int>(n);
+    p.k = static_cast<int>(k);
+    tgemm::Device d;
+    d.sm_count = sm_count;
+    int64_t plan[3];
+    tgemm::ffma_f32_plan(p, d, plan);
+    for (int i = 0; i < 3; ++i) out[i] = plan[i];
+    return TGEMM_OK;
+}
+
 int tgemm_version(void) { return 200; }
 
 int tgemm_debug_build(void) { return tgemm::kDebugBuild ? 1 : 0; }

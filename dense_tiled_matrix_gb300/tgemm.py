@@ -45,6 +45,7 @@ SIGNATURES = {
     "tgemm_kernel_launches": (ctypes.c_uint64, []),
     "tgemm_plan": (ctypes.c_int, [ctypes.c_int, _I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
                                   ctypes.POINTER(ctypes.c_int)]),
+    "tgemm_plan_f32": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.POINTER(ctypes.c_int64)]),
     "tgemm_version": (ctypes.c_int, []),
 }
 
@@ -212,6 +213,13 @@ def tgemm_plan(mode: str, m: int, n: int, k: int, sm_count: int = 152, workspace
     _check(st)
     return {"tile_rows": out[0], "tile_cols": out[1], "stream_k": bool(out[2]), "pieces": out[3],
             "pairs": bool(out[4])}
+
+
+def tgemm_plan_f32(m: int, n: int, k: int, sm_count: int = 152) -> dict:
+    """The 128 x 128 tiles tgemm_f32 would run; see tgemm_plan_f32 in include/tgemm.h."""
+    out = (ctypes.c_int64 * 3)()
+    _check(load().tgemm_plan_f32(m, n, k, sm_count, out))
+    return {"whole_tiles": out[0], "split_tiles": out[1], "pieces": out[2]}
 
 
 def raw(name: str):

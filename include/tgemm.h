@@ -224,6 +224,14 @@ uint64_t tgemm_kernel_launches(void);
  * outside 1 .. 2^31 - 1 or sm_count outside 1 .. 4096. */
 tgemm_status tgemm_plan(int tf32, int64_t m, int64_t n, int64_t k, int sm_count, int workspace, int *out);
 
+/* The same for tgemm_f32 (128 x 128 tiles on the FMA pipes): writes out[0] =
+ * tiles run whole, out[1] = tiles of a partly filled last round that are cut
+ * along k instead, out[2] = pieces per such tile (0: none; their partial sums
+ * are then added in piece order).  Host arithmetic only.  Returns TGEMM_OK, or
+ * TGEMM_ERR_INVALID_VALUE (out untouched) for a NULL out, sizes outside
+ * 1 .. 2^31 - 1 or sm_count outside 1 .. 4096. */
+tgemm_status tgemm_plan_f32(int64_t m, int64_t n, int64_t k, int sm_count, int64_t *out);
+
 /* Library version: major * 10000 + minor * 100 + patch. */
 int tgemm_version(void);
 

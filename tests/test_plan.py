@@ -78,3 +78,40 @@ def test_plan_argument_rules():
     assert list(out) == [7] * 5                      # untouched on a refusal
     assert lib.tgemm_plan(0, 16, 4, 4, 152, 1, out) == tgemm.TGEMM_OK
     assert list(out) == [0] * 5                      # bf16, m <= 64: the cluster split-K kernel
+    out64 = (ctypes.c_int64 * 3)(7, 7, 7)
+    assert lib.tgemm_plan_f32(4, 0, 4, 152, out64) == bad
+    assert lib.tgemm_plan_f32(4, 4, 4, 5000, out64) == bad
+    assert lib.tgemm_plan_f32(4, 4, 4, 152, None) == bad
+    assert list(out64) == [7, 7, 7]
+    assert lib.tgemm_plan_f32(4, 4, 4, 152, out64) == tgemm.TGEMM_OK and list(out64) == [1, 0, 0]
+
+
+def test_fp32_plan_matches_the_restated_split_rule():
+    """tgemm_f32's split of a partly filled last round (tgemm_plan_f32) against
+    test_stream_k_model.split_tail, on named shapes and a seeded sweep of tile
+    counts around multiples of the SM count and k around the piece minimum."""
+    from test_stream_k_model import split_tail
+
+    def library(m, n, k, G):
+        d = tgemm.tgemm_plan_f32(m, n, k, G)
+        return None if d["pieces"] == 0 else (d["whole_tiles"], d["split_tiles"], d["pieces"])
+
+    for shape in [(4096, 4096, 4096), (1024, 1024, 4096), (8192, 8192, 2048), (4097, 3001, 1023),
+                  (8192, 8192, 512), (200, 150, 90), (256, 256, 65536), (2432, 2100, 2050), (1000, 900, 4100),
+                  (500, 20000, 2050), (2000, 2000, 4100), (1024, 1024, 1024)]:
+        assert library(*shape, 152) == split_tail(*shape), shape
+    rng = np.random.default_rng(21)
+    split = 0
+    for _ in range(3000):
+        m = int(rng.integers(1, 9000))
+        n = int(rng.integers(1, 9000))
+        k = int(rng.choice([16, 200, 255, 256, 257, 511, 1024, 4100, 70000]))
+        G = int(rng.choice([152, 148, 132]))
+        want = split_tail(m, n, k, G)
+        assert library(m, n, k, G) == want, (m, n, k, G)
+        if want is None:
+            d = tgemm.tgemm_plan_f32(m, n, k, G)
+            assert d["whole_tiles"] == -(-m // 128) * -(-n // 128) and d["split_tiles"] == 0
+        else:
+            split += 1
+    assert 300 < split < 2700     # both kinds of plan were reached
