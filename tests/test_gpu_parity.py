@@ -76,6 +76,8 @@ MID_K_WIDE_SHAPES = [(2048, 4864, 1024), (2900, 5000, 1030)]
 def test_mid_k_wide_tiles(mode, shape):
     m, n, k = shape
     assert launch_rules.tile_rows(m, n, k, mode) == 256
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert tgemm.tgemm_plan(mode, m, n, k, sm)["tile_rows"] == 256
     parity.full_check(mode, inputs.random_case(5100 + m + n + k, m, n, k, kind="int"), f"{mode} int {shape}")
     parity.full_check(mode, inputs.random_case(6100 + m + n + k, m, n, k, kind="uniform"), f"{mode} uniform {shape}")
 
@@ -98,6 +100,8 @@ SPLIT_SHAPES = [(2432, 2100, 2050), (1000, 900, 4100), (500, 20000, 2050), (2000
 @pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_fp32_split_remainder(shape):
     m, n, k = shape
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert tgemm.tgemm_plan_f32(m, n, k, sm)["pieces"] >= 2   # this device splits the last round
     parity.full_check("f32", inputs.random_case(7000 + m + n + k, m, n, k, kind="int"), f"f32 int {shape}")
     case = inputs.random_case(8000 + m + n + k, m, n, k, kind="uniform")
     parity.full_check("f32", case, f"f32 uniform {shape}")
@@ -115,6 +119,8 @@ UMMA_SK_SHAPES = [(3300, 3000, 3100), (2000, 2600, 1000), (2600, 4000, 4100)]
 @pytest.mark.parametrize("shape", UMMA_SK_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_tensor_core_split_tiles(mode, shape):
     m, n, k = shape
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert tgemm.tgemm_plan(mode, m, n, k, sm)["stream_k"]   # this device takes stream-K here
     parity.full_check(mode, inputs.random_case(9000 + m + n + k, m, n, k, kind="int"), f"{mode} int {shape}")
     case = inputs.random_case(9500 + m + n + k, m, n, k, kind="uniform")
     parity.full_check(mode, case, f"{mode} uniform {shape}")
@@ -420,6 +426,8 @@ PIECE_SHAPES = [(1024, 1024, 8192), (65, 4096, 4096), (1000, 1001, 2000), (129, 
 def test_split_k_pieces(mode, shape):
     m, n, k = shape
     assert launch_rules.pieces(m, n, k, mode) >= 2
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert tgemm.tgemm_plan(mode, m, n, k, sm)["pieces"] >= 2
     parity.full_check(mode, inputs.random_case(8400 + m + n + k, m, n, k, kind="int"), f"{mode} pieces int {shape}")
     case = inputs.random_case(8500 + m + n + k, m, n, k, kind="uniform")
     parity.full_check(mode, case, f"{mode} pieces uniform {shape}")
