@@ -110,7 +110,7 @@ __device__ __forceinline__ void tile_coords(int tile, int tiles_m, int tiles_n, 
     tn = in_group / rows;
 }
 
-// Named barrier of the four epilogue warps (threads 64 .. 191).
+// Named barrier of the epilogue warps (threads 64 .. 64 + 32 kEpiWarps - 1).
 template <int kEpiWarps>
 __device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, %0;" :: "n"(32 * kEpiWarps) : "memory"); }
 
@@ -120,7 +120,9 @@ __device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, %0;"
 // split tile stores its fp32 accumulator in its CTA's `ws` slot and raises
 // its flag; the head waits for the flag, adds that partial to its own
 // accumulator (always head + tail) and stores the tile.  Split tiles need
-// every CTA resident: the launch is cooperative.
+// every CTA resident: the launch is cooperative.  With kSK and pieces > 0 the
+// grid has one CTA per split-K piece instead, each storing its partial tile
+// in its own `ws` slot for umma_pieces_reduce_kernel; nothing waits then.
 template <bool kTF32, bool kBKMajor, bool kWide, int kBN, bool kSK, bool kPair, int kEpiWarps>
 __global__ void __launch_bounds__(threads_for(kEpiWarps), 1)
 umma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
