@@ -66,6 +66,7 @@ GB300 = dict(max_threads=2048, max_blocks=32, smem_per_sm=228 * 1024, regs_per_s
     ("umma_kernel, 4 epilogue warps", 192, 230512, 128, 1),   # 192 KiB ring + 32 KiB staging
     ("umma_kernel, 8 epilogue warps", 320, 230512, 128, 1),   # 75-127 registers
     ("umma_skinny_kernel<16>", 128, 74840, 32, 3),
+    ("umma_pieces_reduce_kernel", 256, 0, 40, 6),     # register-limited: 65536 / (256 x 40)
     ("transpose_tma_kernel", 256, 99360, 40, 2),
 ])
 def test_libtgemm_kernels(name, threads, smem, regs, expect):
