@@ -300,3 +300,77 @@ def test_umma_stream_k_shapes(mode):
         per_cta = segments_of(tiles, kt, G)
         assert sum(roles(s, kt).count("head") for s in per_cta) > 20
     assert not umma_choice(1024, 1024, 1024, mode)[3]   # fewer tiles than SMs
+
+
+# ---- split-K pieces of the tcgen05 kernels: slot layout and reduce, simulated ----
+def _slot_of(part, bm, bn):
+    """A piece's partial tile (bm x bn) in the workspace slot layout the
+    epilogue writes: float4 ((h * bn/32 + c) * 8 + q) * 128 + r = columns
+    32c + 4q .. +3 of row 128h + r."""
+    slot = np.empty((bm * bn // 4, 4), np.float32)
+    for h in range(bm // 128):
+        for c in range(bn // 32):
+            for q in range(8):
+                f0 = ((h * (bn // 32) + c) * 8 + q) * 128
+                slot[f0:f0 + 128] = part[128 * h:128 * h + 128, 32 * c + 4 * q:32 * c + 4 * q + 4]
+    return slot
+
+
+def _reduce(slots, tiles_m, tiles_n, M, N, bm, bn, group_m, pieces):
+    """umma_pieces_reduce_kernel's index arithmetic: block (t, j), thread i,
+    float4 f = 1024 j + 256 r + i; the pieces added in order; rows and columns
+    past C skipped.  Returns C and how often each element was written."""
+    C = np.full((M, N), np.nan, np.float32)
+    writes = np.zeros((M, N), np.int64)
+    k4 = bm * bn // 4
+    for t in range(tiles_m * tiles_n):
+        per_group = group_m * tiles_n
+        g, first = t // per_group, (t // per_group) * group_m
+        rows_g = min(tiles_m - first, group_m)
+        tm, tn = first + (t - g * per_group) % rows_g, (t - g * per_group) // rows_g
+        v = slots[t * pieces].copy()
+        for p in range(1, pieces):
+            v += slots[t * pieces + p]
+        for f in range(k4):
+            gq = f >> 7
+            q, hc = gq & 7, gq >> 3
+            row = tm * bm + (hc // (bn // 32)) * 128 + (f & 127)
+            col = tn * bn + (hc % (bn // 32)) * 32 + q * 4
+            if row >= M:
+                continue
+            for j in range(4):
+                if col + j < N:
+                    C[row, col + j] = v[f, j]
+                    writes[row, col + j] += 1
+    return C, writes
+
+
+@pytest.mark.parametrize("bm, M, N, group_m", [(256, 300, 520, 8), (128, 257, 300, 16)])
+def test_split_k_pieces_slot_layout_and_reduce(bm, M, N, group_m):
+    """The pieces of every tile, stored in the epilogue's slot layout and added
+    by the reduce's index map in piece order, give A @ B exactly (integer
+    inputs), with every element of C written once and nothing outside it."""
+    bn, bk, pieces = 256, 64, 3
+    K = 5 * bk + 17                                   # ragged k: the last phase partly zero-filled
+    rng = np.random.default_rng(3)
+    A = rng.integers(-3, 4, (M, K)).astype(np.float32)
+    B = rng.integers(-3, 4, (K, N)).astype(np.float32)
+    tiles_m, tiles_n = -(-M // bm), -(-N // bn)
+    kt = -(-K // bk)
+    Ap = np.zeros((tiles_m * bm, kt * bk), np.float32)
+    Ap[:M, :K] = A
+    Bp = np.zeros((kt * bk, tiles_n * bn), np.float32)
+    Bp[:K, :N] = B
+    slots = []
+    for t in range(tiles_m * tiles_n):
+        per_group = group_m * tiles_n
+        g, first = t // per_group, (t // per_group) * group_m
+        rows_g = min(tiles_m - first, group_m)
+        tm, tn = first + (t - g * per_group) % rows_g, (t - g * per_group) // rows_g
+        for p in range(pieces):
+            ka, kz = kt * p // pieces * bk, kt * (p + 1) // pieces * bk
+            part = Ap[tm * bm:(tm + 1) * bm, ka:kz] @ Bp[ka:kz, tn * bn:(tn + 1) * bn]
+            slots.append(_slot_of(part, bm, bn))
+    C, writes = _reduce(slots, tiles_m, tiles_n, M, N, bm, bn, group_m, pieces)
+    assert np.array_equal(writes, np.ones((M, N), np.int64))
+    np.testing.assert_array_equal(C, A @ B)
