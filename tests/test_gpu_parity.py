@@ -442,6 +442,8 @@ def test_split_k_pieces_with_unaligned_c(mode):
     reduce kernel's scalar stores; NaN guard columns must stay untouched."""
     m, n, k = 1000, 1001, 2000
     assert launch_rules.pieces(m, n, k, mode) >= 2
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert tgemm.tgemm_plan(mode, m, n, k, sm)["pieces"] >= 2
     case = inputs.random_case(8600, m, n, k, kind="int")
     A_np, B_np = parity.inputs_for(mode, case)
     ldc = n + 1
