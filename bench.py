@@ -129,6 +129,17 @@ def traffic_table(path=TRAFFIC_TABLE):
     return out
 
 
+def plan_of(entry, m, n, k, sm_count):
+    """The tiles libtgemm picks for a shape (tgemm_plan / tgemm_plan_f32: host
+    arithmetic), or None for the pages' comparator kernels."""
+    from dense_tiled_matrix_gb300 import tgemm
+    if entry == "f32":
+        return tgemm.tgemm_plan_f32(m, n, k, sm_count)
+    if entry in ("tf32", "bf16"):
+        return tgemm.tgemm_plan(entry, m, n, k, sm_count)
+    return None
+
+
 def fp32_peak(sm_count, sm_max_mhz):
     """(TFLOP/s, derivation) of the FP32 FMA peak: SMs x lanes x 2 flop x max SM clock."""
     tf = sm_count * FP32_LANES_PER_SM * 2 * sm_max_mhz * 1e6 / 1e12
@@ -481,6 +492,9 @@ def bench_tgemm(args, world, rank, local):
                        "ms": round(med * 1e3, 4), "ms_mean": round(sum(ts) / len(ts) * 1e3, 4),
                        "tflops": round(2.0 * c.m * c.n * c.k / med / 1e12, 2),
                        "roofline": roof_part}
+        plan = plan_of(entry, c.m, c.n, c.k, sm_count)
+        if plan is not None:
+            parts[name]["plan"] = plan
         if name in b2b:
             # informational: `ms`, `tflops` and the roofline use the per-launch event pairs
             parts[name]["ms_back_to_back"] = round(b2b[name] * 1e3, 4)

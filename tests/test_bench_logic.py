@@ -124,3 +124,18 @@ def test_every_bench_shape_names_a_workload_and_an_entry():
     assert sizes["long_k"] == (1024, 1024, 8192)
     for mode in ("bf16", "tf32"):
         assert launch_rules.pieces(*sizes["long_k"], mode) >= 2
+
+
+def test_plan_of_each_entry():
+    """bench.plan_of reports libtgemm's own plan for the shapes it times
+    (host arithmetic, no GPU): FFMA split remainder at 4096^3, wide tiles at
+    8192^3, TF32 224-wide tiles at 4096^3, split-K pieces at 1024 x 1024 x 8192;
+    nothing for the pages' kernels."""
+    from dense_tiled_matrix_gb300 import build as tbuild
+    tbuild.build()
+    assert bench.plan_of("f32", 4096, 4096, 4096, 152) == {"whole_tiles": 912, "split_tiles": 112, "pieces": 4}
+    assert bench.plan_of("bf16", 8192, 8192, 8192, 152)["tile_rows"] == 256
+    assert bench.plan_of("tf32", 4096, 4096, 4096, 152)["tile_cols"] == 224
+    assert bench.plan_of("bf16", 1024, 1024, 8192, 152)["pieces"] == 9
+    assert bench.plan_of("bf16", 16, 8192, 8192, 152)["tile_rows"] == 0    # the cluster split-K kernel
+    assert bench.plan_of("pages_naive", 1024, 1024, 1024, 152) is None
